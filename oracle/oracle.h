@@ -1,0 +1,60 @@
+/*
+ * Reference oracle for paged decode attention (fp64, CPU).
+ * TEST INFRASTRUCTURE ONLY: used by the tests, the smoke check and the
+ * benchmark's CPU-baseline leg, never by the library.
+ *
+ * All arrays are host memory, row-major and contiguous:
+ *   q            bf16 bits [num_seqs, num_q_heads, head_dim]
+ *   k, v         bf16 bits [num_tokens, num_kv_heads, head_dim]
+ *   k_cache,
+ *   v_cache      bf16 bits [num_blocks, block_size, num_kv_heads, head_dim]
+ *   slot_mapping int64 [num_tokens]; -1 = skip, else block * block_size + offset
+ *   block_tables int32 [num_seqs, max_blocks_per_seq]
+ *   context_lens int32 [num_seqs]
+ *   out          double [num_seqs, num_q_heads, head_dim]
+ */
+#ifndef PAGED_DECODE_ORACLE_H
+#define PAGED_DECODE_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum { ORACLE_OK = 0, ORACLE_ERR_ARG = 1, ORACLE_ERR_RANGE = 2 };
+
+/* Copy row i of k and v to cache slot slot_mapping[i]; -1 rows are skipped.
+ * Nothing is written if any slot is out of range. */
+int oracle_store_kvcache(const uint16_t *k, const uint16_t *v,
+                         uint16_t *k_cache, uint16_t *v_cache,
+                         const int64_t *slot_mapping, int64_t num_tokens,
+                         int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks);
+
+/* softmax(q K^T * scale) V per (sequence, query head) over the sequence's
+ * context_lens[s] tokens, gathered through its block table.
+ * num_threads <= 0 uses every OpenMP thread. */
+int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                  const int32_t *block_tables, int max_blocks_per_seq,
+                  const int32_t *context_lens, double scale, double *out,
+                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                  int block_size, int64_t num_blocks, int num_threads);
+
+/* The same, for the listed (sequence, query head) pairs only:
+ * pairs int32 [num_pairs, 2], out double [num_pairs, head_dim]. */
+int oracle_decode_pairs(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *context_lens, double scale,
+                        const int32_t *pairs, int64_t num_pairs, double *out,
+                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int block_size, int64_t num_blocks, int num_threads);
+
+/* Threads the OpenMP loops use by default. */
+int oracle_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif

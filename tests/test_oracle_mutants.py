@@ -1,0 +1,45 @@
+"""Plant plausible mistakes in copies of the oracle source and check that
+every one of them fails at least one pin. CPU only."""
+import os
+
+import pytest
+
+import oracle
+
+import pins
+
+SRC = os.path.join(os.path.dirname(oracle.__file__), "oracle.c")
+
+# (name, text in oracle.c, replacement); every mutant stays in bounds
+MUTANTS = [
+    ("kv_head_modulo", "const int kvh = h / group;", "const int kvh = h % num_kv_heads;"),
+    ("head_major_layout", "((block * block_size + t % block_size) * num_kv_heads + kvh)",
+     "((block * num_kv_heads + kvh) * block_size + t % block_size)"),
+    ("rows_reversed", "(block * block_size + t % block_size)",
+     "(block * block_size + (block_size - 1 - t % block_size))"),
+    ("scale_dropped", "score[t] = scale * dot;", "score[t] = dot;"),
+    ("not_normalised", "double p = score[t] / denom;", "double p = score[t];"),
+    ("last_token_dropped", "t < L;", "t < L - 1;"),
+    ("query_row_of_kv_head", "(int64_t)s * num_q_heads + h) * head_dim",
+     "(int64_t)s * num_q_heads + kvh) * head_dim"),
+    ("store_v_from_k", "memcpy(v_cache + slot * row, v + i * row",
+     "memcpy(v_cache + slot * row, k + i * row"),
+    ("store_skips_first_row", "if (slot == -1)\n            continue;",
+     "if (slot == -1 || i == 0)\n            continue;"),
+]
+
+
+@pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
+def test_mutant_is_caught(tmp_path, name, old, new):
+    text = open(SRC).read()
+    assert old in text, f"mutation anchor for {name} not found"
+    src = tmp_path / "mutant.c"
+    src.write_text(text.replace(old, new))
+    mutant = oracle.compile_variant(str(src), str(tmp_path / "libmutant.so"))
+    failed = []
+    for pin in pins.ALL_PINS:
+        try:
+            pin(mutant)
+        except (AssertionError, oracle.OracleError) as e:
+            failed.append((pin.__name__, str(e)[:80]))
+    assert failed, f"mutant {name} passed every pin"
