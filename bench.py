@@ -1,0 +1,378 @@
+"""Benchmark: one paged decode step (store_kvcache of the step's new K/V rows,
+then decode attention) on synthetic inputs, timed with CUDA events.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
+
+Prints one JSON line (rank 0). ``value`` is microseconds per step (store +
+decode, inputs resident in HBM, L2 flushed between steps); ``roofline``
+reports the decode launch's KV-read bandwidth against the measured HBM copy
+peak; ``e2e`` repeats the step through host buffers (pinned H2D of the step's
+inputs and D2H of its output inside the timed region); ``cpu_baseline`` times
+the fp64 CPU oracle on a bounded sample of the same step and scales it to a
+full step. ``--impl reference`` times only that oracle (the reference arm).
+With N > 1 (torchrun) every rank runs its own replica of the step on its own
+GPU: the path has no cross-GPU exchange.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from paged_kv_cache_255_gb300 import inputs  # noqa: E402
+
+METRIC = "paged-decode µs/step and KV-read GB/s (fraction of GB300 HBM peak)"
+DEFAULT_WORKLOAD = "qwen3_0_6b"
+L2_FLUSH_BYTES = 512 << 20       # > 2x the 129 MB L2
+FALLBACK_HBM_GBS = 6800.0
+PROFILE_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
+KERNEL_SOURCES = ["paged_kv_cache_255_gb300/csrc/decode.cu", "paged_kv_cache_255_gb300/csrc/common.cuh"]
+
+
+def kernel_hash() -> str:
+    h = hashlib.sha256()
+    for p in KERNEL_SOURCES:
+        with open(os.path.join(ROOT, p), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def ncu_traffic(workload: str):
+    """DRAM bytes per decode launch from the committed ncu summary, if it was
+    taken on this workload with the current kernel source."""
+    try:
+        text = open(PROFILE_FILE).read()
+    except OSError:
+        return None
+    want = kernel_hash()
+    for m in re.finditer(r"^traffic\s+workload=(\S+)\s+kernel_hash=(\S+)\s+bytes_per_launch=(\d+)",
+                         text, re.M):
+        if m.group(1) == workload and m.group(2) == want:
+            return int(m.group(3))
+    return None
+
+
+class ClockSampler:
+    """nvidia-smi clock and throttle-reason samples while the GPU is busy."""
+
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
+              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
+              "clocks_event_reasons.sw_power_cap"]
+
+    def __init__(self, index: int):
+        self.proc = None
+        self.path = None
+        try:
+            fd, self.path = tempfile.mkstemp(prefix="clocks", suffix=".csv")
+            os.close(fd)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu=timestamp,{','.join(self.FIELDS)}",
+                 "--format=csv,noheader,nounits", "-lms", "100", "-i", str(index)],
+                stdout=self.fh, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) != 1 + len(self.FIELDS):
+                continue
+            try:
+                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
+            except ValueError:
+                continue
+        os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+                          if f.lower() == "active"})
+        return {"sm_mhz": statistics.median(r[0] for r in rows),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+
+
+def dist_setup(n_gpus):
+    if n_gpus <= 1 and "RANK" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    rank = int(os.environ.get("RANK", 0))
+    world = int(os.environ.get("WORLD_SIZE", n_gpus))
+    local = int(os.environ.get("LOCAL_RANK", rank))
+    backend = "nccl" if torch.cuda.is_available() else "gloo"
+    if torch.cuda.is_available():
+        torch.cuda.set_device(local)
+    dist.init_process_group(backend=backend)
+    return rank, world, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda" if torch.cuda.is_available() else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def workload_config(wl):
+    s = wl.spec
+    return {"workload": s.name, "num_seqs": wl.num_seqs, "num_q_heads": s.num_q_heads,
+            "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
+            "num_blocks": wl.num_blocks, "store_rows": int(wl.slot_mapping.shape[0]),
+            "context_tokens": int(wl.context_lens.astype(np.int64).sum()),
+            "max_context_len": wl.max_context_len, "seed": wl.seed,
+            "l2": "flushed between steps (512 MiB write)"}
+
+
+def oracle_sample(wl, target_s: float, host=None):
+    """Time the fp64 oracle on a bounded sample of the step and scale to a full
+    step. Returns (us_per_step, threads, sample description)."""
+    import oracle
+    O = oracle.get()
+    threads = O.num_threads()
+    if host is None:
+        host = (wl.q.cpu(), wl.k_cache.cpu(), wl.v_cache.cpu(), wl.k_new.cpu(), wl.v_new.cpu())
+    q, kc, vc, kn, vn = host
+    t_store = 0.0
+    if wl.slot_mapping.shape[0]:
+        kc = oracle._bits(kc).copy()            # private pools for the in-place store (untimed)
+        vc = oracle._bits(vc).copy()
+        t0 = time.perf_counter()
+        O.store_kvcache_into(kn, vn, kc, vc, wl.slot_mapping)
+        t_store = time.perf_counter() - t0
+    S, Hq = wl.num_seqs, wl.spec.num_q_heads
+    work_all = float(wl.context_lens.astype(np.float64).sum()) * Hq
+    rng = np.random.Generator(np.random.PCG64(123))
+    order = rng.permutation(S * Hq)
+    done_pairs, done_work, elapsed = 0, 0.0, 0.0
+    batch = max(threads, 8)
+    while elapsed < target_s and done_pairs < S * Hq:
+        idx = order[done_pairs:done_pairs + batch]
+        pairs = np.stack([idx // Hq, idx % Hq], 1).astype(np.int32)
+        t0 = time.perf_counter()
+        O.decode_pairs(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale, pairs, threads=0)
+        elapsed += time.perf_counter() - t0
+        done_pairs += len(idx)
+        done_work += float(wl.context_lens[idx // Hq].astype(np.float64).sum())
+        batch = min(batch * 2, 4096)
+    decode_s = elapsed * (work_all / max(done_work, 1.0))
+    us = (t_store + decode_s) * 1e6
+    sample = (f"oracle store of all {int(wl.slot_mapping.shape[0])} rows + decode of "
+              f"{done_pairs}/{S * Hq} random (seq, q-head) outputs ({elapsed:.1f} s), scaled by "
+              f"context tokens to the full step")
+    return us, threads, sample
+
+
+def workload_spec(args):
+    spec = inputs.SPECS[args.workload]
+    if args.num_seqs:
+        spec = inputs.scaled(spec, num_seqs=args.num_seqs, name=f"{spec.name}_s{args.num_seqs}")
+    return spec
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return
+    wl = inputs.generate(workload_spec(args), seed=0,
+                         device="cuda" if torch.cuda.is_available() else "cpu")
+    host = (wl.q.cpu(), wl.k_cache.cpu(), wl.v_cache.cpu(), wl.k_new.cpu(), wl.v_new.cpu())
+    per_step = max(1.0, args.ref_seconds / max(1, args.steps))
+    for _ in range(args.warmup):
+        oracle_sample(wl, 0.2, host)
+    vals = []
+    for _ in range(args.steps):
+        us, threads, sample = oracle_sample(wl, per_step, host)
+        vals.append(us)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us/step",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": workload_config(wl),
+            "cpu_baseline": {"value": v, "unit": "us/step", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu(args, rank, world, local):
+    from paged_kv_cache_255_gb300 import pagedattn as pa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    wl = inputs.generate(workload_spec(args), seed=0, device=dev)
+    S, Hq, Hkv, D = wl.num_seqs, wl.spec.num_q_heads, wl.spec.num_kv_heads, wl.spec.head_dim
+    q = wl.q
+    k_cache, v_cache = wl.k_cache, wl.v_cache
+    k_new, v_new = wl.k_new, wl.v_new
+    slots = torch.from_numpy(wl.slot_mapping).to(dev)
+    bt = torch.from_numpy(wl.block_tables).to(dev)
+    cl = torch.from_numpy(wl.context_lens).to(dev)
+    out = torch.empty_like(q)
+    ws = pa.workspace_for(Hq, Hkv, D, 0, dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    has_store = slots.shape[0] > 0
+
+    def step():
+        if has_store:
+            pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots)
+        pa.decode(q, k_cache, v_cache, bt, cl, wl.scale, out=out, workspace=ws)
+
+    # ---- device-resident timing
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        if has_store:
+            pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots)
+        ev[i][1].record(stream)
+        pa.decode(q, k_cache, v_cache, bt, cl, wl.scale, out=out, workspace=ws)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    store_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world)
+    dec_avg = max_over_ranks(sum(dec_ms) / len(dec_ms), world)
+    store_avg = max_over_ranks(sum(store_ms) / len(store_ms), world)
+
+    # ---- end to end through host buffers
+    hq = q.cpu().pin_memory()
+    hk, hv = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
+    hs = slots.cpu().pin_memory()
+    hbt, hcl = bt.cpu().pin_memory(), cl.cpu().pin_memory()
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
+    ds, dbt, dcl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(cl)
+    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hbt, hcl))
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (ds, hs), (dbt, hbt), (dcl, hcl)):
+            d_.copy_(h_, non_blocking=True)
+        if has_store:
+            pa.store_kvcache(dk, dv, k_cache, v_cache, ds)
+        pa.decode(dq, k_cache, v_cache, dbt, dcl, wl.scale, out=out, workspace=ws)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        e2e_step()
+        b_.record(stream)
+        b_.synchronize()
+        e2e_ms.append(a_.elapsed_time(b_))
+    e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+
+    if rank != 0:
+        return
+    kv_bytes = wl.kv_bytes()
+    peak, peak_src = measured_peaks()
+    achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
+    line = {
+        "metric": METRIC, "value": ms * 1e3, "unit": "us/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": workload_config(wl),
+        "store_us": store_avg * 1e3, "decode_us": dec_avg * 1e3,
+        "kv_read_gbs": achieved, "hbm_frac": achieved / peak,
+        "unique_kv_read_gbs": wl.unique_kv_bytes() / (dec_avg * 1e-3) / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": ncu_traffic(wl.spec.name),
+                     "kernel": "pa_decode (decode + combine launches)",
+                     "algorithmic_bytes": kv_bytes, "peak_source": f"{peak_src} hbm_gbs"},
+        "e2e": {"value": e2e * 1e3, "unit": "us/step", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * (3 if has_store else 2),
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline and world >= 1:
+        us, threads, sample = oracle_sample(wl, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": us, "unit": "us/step", "cores": threads,
+                                "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.SPECS))
+    ap.add_argument("--num-seqs", type=int, default=0,
+                    help="run a copy of the workload with this many sequences (profiling)")
+    ap.add_argument("--impl", default="native", choices=["native", "reference"])
+    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--ref-seconds", type=float, default=60.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    rank, world, local = dist_setup(args.gpus)
+    if args.impl == "reference":
+        run_reference(args, rank, world)
+    else:
+        if not torch.cuda.is_available():
+            raise SystemExit("bench.py needs a CUDA device")
+        run_gpu(args, rank, world, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,150 @@
+/*
+ * libpagedattn -- paged KV-cache store and single-token decode attention,
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * The operations follow the pages that describe a minimal vLLM engine:
+ *   - KV is kept in fixed-size token blocks of one pool
+ *     ("Building a minimal vLLM implementation", config.py, kvcache_block_size);
+ *   - each sequence's block_table maps its logical blocks to physical blocks
+ *     (same page, sequence.py, block_table);
+ *   - block 0 of the pool is a reserved null block that no sequence owns
+ *     ("Implementation Details", PagedAttention -- BlockPool);
+ *   - decode runs one new token per sequence (sequence.py __getstate__:
+ *     in decode only the last token is sent to the workers);
+ *   - the decode kernel is the engine's paged-attention kernel
+ *     ("A vLLM engine small enough to read in one sitting", What it does /
+ *     Key highlights: paged attention for decoding).
+ *
+ * Layouts (all row-major, contiguous, bf16 = IEEE bfloat16):
+ *   q            [num_seqs, num_q_heads, head_dim]                 bf16
+ *   k, v         [num_tokens, num_kv_heads, head_dim]              bf16
+ *   k_cache,
+ *   v_cache      [num_blocks, block_size, num_kv_heads, head_dim]  bf16
+ *   slot_mapping [num_tokens] int64; slot = block * block_size + offset, -1 = skip
+ *   block_tables [num_seqs, max_blocks_per_seq] int32 physical block ids
+ *   context_lens [num_seqs] int32, tokens of each sequence, counting the one
+ *                just stored
+ *   out          [num_seqs, num_q_heads, head_dim]                 bf16
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ *
+ * Ownership: every pointer is caller-owned memory on the current CUDA device
+ * (the workspace included). The library allocates nothing and keeps no state
+ * between calls. Calls are asynchronous on `stream` (a cudaStream_t; NULL is
+ * the legacy default stream) and return once the kernels are queued.
+ *
+ * Errors: argument problems are found on the host, before anything is
+ * launched, and returned as a status. Index values the kernels read on the
+ * device (slots, block ids, lengths) are never trusted for addressing: a slot
+ * outside [-1, num_blocks * block_size) writes nothing, a block id outside
+ * [0, num_blocks) contributes no tokens, a length is clamped to
+ * [0, max_blocks_per_seq * block_size]. Such inputs give unspecified output
+ * values but never touch memory outside the buffers passed in.
+ */
+#ifndef PAGEDATTN_H
+#define PAGEDATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PA_API __attribute__((visibility("default")))
+#else
+#define PA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PA_OK = 0,
+    PA_ERR_INVALID_ARG = 1,   /* null pointer, bad size, misaligned buffer */
+    PA_ERR_UNSUPPORTED = 2,   /* head_dim != 128, block_size, group size   */
+    PA_ERR_WORKSPACE = 3,     /* workspace missing or too small            */
+    PA_ERR_CUDA = 4           /* a CUDA call or launch failed              */
+} pa_status_t;
+
+/* Human-readable name of a status. Never NULL. */
+PA_API const char *pa_status_string(pa_status_t status);
+
+/*
+ * Store new K/V rows into the paged cache.
+ *
+ * For every i < num_tokens with slot_mapping[i] != -1:
+ *   k_cache viewed as [num_blocks * block_size, num_kv_heads * head_dim],
+ *   row slot_mapping[i], becomes k[i]; the same for v / v_cache.
+ * Rows with slot -1 (batch padding) write nothing. The copy is bit-exact.
+ * Two rows with the same slot: the value left there is unspecified.
+ *
+ * This is how a decode step puts the token it has just projected into the
+ * block its sequence's block_table names (the write side of the paged KV
+ * cache, "A vLLM engine small enough to read in one sitting": paged KV cache
+ * management).
+ *
+ * Requirements: head_dim == 128; block_size a power of two in [16, 256];
+ * all pointers 16-byte aligned (non-null unless num_tokens == 0).
+ */
+PA_API pa_status_t pa_store_kvcache(const void *k, const void *v,
+                             void *k_cache, void *v_cache,
+                             const int64_t *slot_mapping, int64_t num_tokens,
+                             int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks, void *stream);
+
+/*
+ * Bytes of device workspace pa_decode needs on the current device for this
+ * head configuration, with num_partitions = 0 (automatic) or a forced count
+ * (see pa_decode_splitk). Returns 0 for an unsupported configuration.
+ */
+PA_API size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
+                                int num_partitions);
+
+/*
+ * Single-token decode attention over the paged cache.
+ *
+ * For each sequence s and query head h, with L = context_lens[s],
+ * kvh = h / (num_q_heads / num_kv_heads) and, for t < L,
+ *   K_t = k_cache[block_tables[s][t / block_size]][t % block_size][kvh]
+ *   V_t = v_cache[ ... same ... ]:
+ *   out[s][h] = sum_t softmax_t(scale * q[s][h] . K_t) V_t
+ * computed in fp32 from the bf16 inputs and rounded to bf16. L == 0 gives 0.
+ * Only the first ceil(L / block_size) entries of a table row are read, and
+ * within the last block only its first L - (blocks - 1) * block_size rows.
+ *
+ * The work is cut into contiguous, equal shares of all sequences' 16-token
+ * tiles (split-K / flash-decoding); a (sequence, KV head) whose tiles span
+ * several shares is finished by a log-sum-exp combine launched after the main
+ * kernel on the same stream. The workspace holds those partial results; its
+ * contents need no initialisation and are garbage after the call.
+ *
+ * Requirements: head_dim == 128; num_q_heads % num_kv_heads == 0 with group
+ * size num_q_heads / num_kv_heads <= 16; block_size a power of two in
+ * [16, 256]; q, k_cache, v_cache, out 16-byte aligned; workspace of at least
+ * pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim, 0) bytes,
+ * 16-byte aligned.
+ */
+PA_API pa_status_t pa_decode(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, float scale, void *out,
+                      int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                      int block_size, int64_t num_blocks,
+                      void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * pa_decode with the number of partitions (split-K shares) forced to
+ * num_partitions >= 1 instead of chosen from the device; num_partitions == 0
+ * is pa_decode. For tests of the combine path and for tuning. The workspace
+ * must hold pa_decode_workspace_size(..., num_partitions) bytes.
+ */
+PA_API pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, float scale, void *out,
+                             int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                             int block_size, int64_t num_blocks,
+                             void *workspace, size_t workspace_bytes,
+                             int num_partitions, void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PAGEDATTN_H */

@@ -107,6 +107,19 @@ class Oracle:
             raise OracleError(f"oracle_store_kvcache returned {rc}")
         return kc, vc
 
+    def store_kvcache_into(self, k, v, k_cache_bits, v_cache_bits, slot_mapping):
+        """The store, writing into the given uint16 cache arrays in place."""
+        kb, vb = _bits(k), _bits(v)
+        sm = _arr(slot_mapping, np.int64)
+        kc, vc = k_cache_bits, v_cache_bits
+        assert kc.dtype == np.uint16 and vc.dtype == np.uint16
+        assert kc.flags.c_contiguous and vc.flags.c_contiguous and kc.shape == vc.shape
+        NB, bs, Hkv, D = kc.shape
+        rc = self.lib.oracle_store_kvcache(_ptr(kb), _ptr(vb), _ptr(kc), _ptr(vc), _ptr(sm),
+                                           sm.shape[0], Hkv, D, bs, NB)
+        if rc != OK:
+            raise OracleError(f"oracle_store_kvcache returned {rc}")
+
     def decode(self, q, k_cache, v_cache, block_tables, context_lens, scale, threads: int = 0):
         """fp64 [S, Hq, D] attention output over the paged cache."""
         qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)

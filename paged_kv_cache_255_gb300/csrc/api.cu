@@ -1,0 +1,150 @@
+// C ABI of libpagedattn: argument checks on the host, then kernel launches.
+// The public contract is in include/pagedattn.h.
+#include <cmath>
+#include <cstdint>
+
+#include "../../include/pagedattn.h"
+#include "kernels.h"
+
+namespace {
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+int log2_exact(int x) {
+    int l = 0;
+    while ((1 << l) < x) ++l;
+    return (1 << l) == x ? l : -1;
+}
+
+bool block_size_ok(int bs) { return bs >= 16 && bs <= 256 && log2_exact(bs) >= 0; }
+
+int current_sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    return n;
+}
+
+// Shares of the tile space for a call: forced, or from the device.
+int plan_workers(int group_pad, int num_partitions) {
+    if (num_partitions > 0) return num_partitions;
+    const int sms = current_sm_count();
+    return sms > 0 ? pa::decode_default_workers(group_pad, sms) : 0;
+}
+
+pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *context_lens, float scale, void *out, int num_seqs,
+                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                        int64_t num_blocks, void *workspace, size_t workspace_bytes,
+                        int num_partitions, void *stream) {
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 ||
+        max_blocks_per_seq < 0 || num_partitions < 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (head_dim != pa::kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+    const int group = num_q_heads / num_kv_heads;
+    const int gp = pa::decode_group_pad(group);
+    if (gp == 0) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_INVALID_ARG;
+
+    const int P = plan_workers(gp, num_partitions);
+    if (P <= 0) return PA_ERR_CUDA;
+    if (!workspace || !aligned16(workspace) || workspace_bytes < pa::decode_workspace_bytes(gp, P))
+        return PA_ERR_WORKSPACE;
+
+    pa::DecodeArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.out = out;
+    a.num_seqs = num_seqs;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = group;
+    a.block_size_log2 = log2_exact(block_size);
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);   // scale * log2(e)
+    a.num_workers = P;
+    a.min_tiles = num_partitions > 0 ? 1 : pa::kDefaultMinTiles;
+    pa::decode_carve_workspace(a, workspace, gp);
+    const cudaError_t e = pa::launch_decode(a, gp, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(pa_status_t status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+pa_status_t pa_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
+                             const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, void *stream) {
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (head_dim != pa::kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) return PA_OK;
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    const int sms = current_sm_count();
+    if (sms <= 0) return PA_ERR_CUDA;
+    const cudaError_t e = pa::launch_store_kvcache(
+        k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads * head_dim,
+        num_blocks * block_size, sms, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
+                                int num_partitions) {
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        head_dim != pa::kHeadDimPublic || num_partitions < 0)
+        return 0;
+    const int gp = pa::decode_group_pad(num_q_heads / num_kv_heads);
+    if (gp == 0) return 0;
+    const int P = plan_workers(gp, num_partitions);
+    if (P <= 0) return 0;
+    return pa::decode_workspace_bytes(gp, P);
+}
+
+pa_status_t pa_decode(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, float scale, void *out, int num_seqs,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      int64_t num_blocks, void *workspace, size_t workspace_bytes,
+                      void *stream) {
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, workspace, workspace_bytes, 0, stream);
+}
+
+pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, float scale, void *out, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks, void *workspace, size_t workspace_bytes,
+                             int num_partitions, void *stream) {
+    if (num_partitions < 0) return PA_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, workspace, workspace_bytes, num_partitions, stream);
+}
+
+}  // extern "C"

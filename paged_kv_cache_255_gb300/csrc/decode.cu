@@ -1,0 +1,544 @@
+// Paged decode attention: one query token per sequence, K/V gathered through
+// the sequence's block table from a pool of fixed-size blocks.
+//
+// What it computes: for sequence s, query head h, KV head kvh = h / g,
+//   out[s][h] = sum_t softmax_t(scale * q[s][h] . K_t) V_t,  t < context_lens[s],
+// where token t sits in physical block block_tables[s][t / bs], row t % bs
+// ("Building a minimal vLLM implementation", sequence.py block_table;
+// config.py kvcache_block_size). This is the engine's decode-side paged
+// attention ("A vLLM engine small enough to read in one sitting").
+//
+// How the work is cut (GB300 design):
+//   * A sequence's tokens form 16-token tiles; a (sequence, KV head) pair is a
+//     unit of max(1, ceil(L / 16)) tiles. All units, sequence-major, form one
+//     flat tile space of W tiles.
+//   * P workers (one warp each, persistent: P = SMs x resident CTAs x warps)
+//     take equal contiguous shares [w W / P, (w + 1) W / P) of that space, so
+//     every SM streams the same number of bytes whatever the length mix.
+//   * A worker streams its tiles through a private NSTAGE-deep cp.async ring
+//     in shared memory (16-byte zero-filling copies; rows past the sequence
+//     end are never read), computes q.K for all g query heads of the KV head
+//     in fp32, keeps an online softmax (running max in log2 units, running
+//     sum) and accumulates P.V in fp32.
+//   * A unit that lies wholly in one share is written straight to `out`. A
+//     unit cut by share boundaries leaves one partial (o, m, l) per share in
+//     the workspace; the worker holding its first tile records a combine task,
+//     and the combine kernel merges the pieces by log-sum-exp weights
+//     (split-K / flash-decoding).
+// The kernels never wait on one another inside a launch.
+#include <cmath>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kSimtWarps = 4;      // workers per CTA
+constexpr int kSimtStages = 3;     // tiles in flight per worker (ring depth)
+
+__device__ __forceinline__ int clamp_len(const int32_t *cl, int s, int max_len) {
+    int L = __ldg(cl + s);
+    L = L < 0 ? 0 : L;
+    return L > max_len ? max_len : L;
+}
+
+// Tiles of a unit: a zero-length sequence still owns one (empty) tile so that
+// some worker writes its zero output.
+__device__ __forceinline__ int unit_tiles(int L) { return L > 0 ? (L + 15) >> 4 : 1; }
+
+// Position in the flat tile space: sequence, KV head, tile within the unit.
+struct Cursor {
+    int s, kvh, j, nt, L;
+};
+
+__device__ __forceinline__ void cursor_advance(Cursor &c, const DecodeArgs &a, int max_len) {
+    if (++c.j == c.nt) {
+        c.j = 0;
+        if (++c.kvh == a.num_kv_heads) {
+            c.kvh = 0;
+            if (++c.s < a.num_seqs) {
+                c.L = clamp_len(a.context_lens, c.s, max_len);
+                c.nt = unit_tiles(c.L);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ int tile_valid(const Cursor &c) {
+    int v = c.L - (c.j << 4);
+    return v < 0 ? 0 : (v > 16 ? 16 : v);
+}
+
+// Physical block of the tile under the cursor (0 when the tile has no tokens).
+__device__ __forceinline__ int tile_block(const Cursor &c, const DecodeArgs &a) {
+    if (tile_valid(c) == 0) return 0;
+    return __ldg(a.block_tables + (int64_t)c.s * a.max_blocks_per_seq +
+                 ((c.j << 4) >> a.block_size_log2));
+}
+
+// Issue the cp.async copies of one K tile and one V tile (16 rows x 256 B
+// each) into `stage`. Lane l copies 16-byte column (l & 15) of rows
+// (l >> 4) + 2i; each instruction covers two whole 256-byte rows.
+__device__ __forceinline__ void issue_tile(const Cursor &c, int bid, uint8_t *stage,
+                                           const DecodeArgs &a, int lane) {
+    int valid = tile_valid(c);
+    if (bid < 0 || (int64_t)bid >= a.num_blocks) valid = 0;   // never address outside the pool
+    const int off = (c.j << 4) & ((1 << a.block_size_log2) - 1);
+    const int64_t row0 = ((((int64_t)bid << a.block_size_log2) + off) * a.num_kv_heads + c.kvh);
+    const int64_t rstride = (int64_t)a.num_kv_heads * kRowBytes;
+    const char *kb = static_cast<const char *>(a.k_cache) + row0 * kRowBytes;
+    const char *vb = static_cast<const char *>(a.v_cache) + row0 * kRowBytes;
+    const int col = (lane & 15) * 16;
+    const uint32_t dst = smem_u32(stage);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = (lane >> 4) + 2 * i;
+        const bool ok = r < valid;
+        const int64_t o = ok ? r * rstride + col : 0;
+        cp_async_16(dst + r * kRowBytes + col, ok ? kb + o : static_cast<const char *>(a.k_cache),
+                    ok ? 16 : 0);
+        cp_async_16(dst + kTileBytes + r * kRowBytes + col,
+                    ok ? vb + o : static_cast<const char *>(a.v_cache), ok ? 16 : 0);
+    }
+}
+
+// Sum NV per-lane values across the 32 lanes, halving the set at each of the
+// five xor steps: afterwards lane l holds max(1, NV / 32) fully reduced
+// values, originally at indices (l >> (5 - log2 NV)) ... for NV < 32 and
+// l * NV / 32 + i for NV >= 32.
+template <int NV>
+__device__ __forceinline__ void butterfly_sum(float (&v)[NV], int lane) {
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+        const int mask = 16 >> step;
+        const int n = NV >> step;
+        if (n >= 2) {
+            const bool upper = lane & mask;
+#pragma unroll
+            for (int i = 0; i < n / 2; ++i) {
+                const float send = upper ? v[i] : v[i + n / 2];
+                const float keep = upper ? v[i + n / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, mask);
+            }
+        } else {
+            v[0] += __shfl_xor_sync(0xffffffffu, v[0], mask);
+        }
+    }
+}
+
+template <int GP, int WARPS, int NSTAGE>
+struct SimtLayout {
+    static constexpr int kStageBytes = 2 * kTileBytes;               // K tile then V tile
+    static constexpr int kScratchFloats = 16 * GP + 2 * GP;          // p[16][GP], alpha, l
+    static constexpr int kScratchBytes = ((kScratchFloats * 4 + 127) / 128) * 128;
+    static constexpr int kWarpBytes = NSTAGE * kStageBytes + kScratchBytes;
+    static constexpr int kCtaBytes = WARPS * kWarpBytes;
+};
+
+// CTA prologue shared by the decode kernels: the total tile count W and the
+// position (sequence, KV head, tile) of this warp's first tile.
+template <int WARPS>
+__device__ __forceinline__ void plan_share(const DecodeArgs &a, int max_len, int64_t &W,
+                                           int &p_eff, int64_t &T0, int64_t &T1, Cursor &c) {
+    __shared__ long long s_wsum[WARPS];
+    __shared__ long long s_scan[WARPS * 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = a.num_seqs, Hkv = a.num_kv_heads;
+
+    // pass 1: total tiles
+    long long local = 0;
+    for (int s = threadIdx.x; s < S; s += WARPS * 32) local += unit_tiles(clamp_len(a.context_lens, s, max_len));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) local += __shfl_xor_sync(0xffffffffu, local, m);
+    if (lane == 0) s_wsum[warp] = local;
+    __syncthreads();
+    long long total = 0;
+#pragma unroll
+    for (int i = 0; i < WARPS; ++i) total += s_wsum[i];
+    __syncthreads();
+    W = total * Hkv;
+
+    int64_t pe = W / (a.min_tiles > 0 ? a.min_tiles : 1);
+    if (pe < 1) pe = 1;
+    if (pe > a.num_workers) pe = a.num_workers;
+    p_eff = (int)pe;
+    const int w = blockIdx.x * WARPS + warp;
+    if (w < p_eff) {
+        T0 = (int64_t)w * W / p_eff;
+        T1 = (int64_t)(w + 1) * W / p_eff;
+    } else {
+        T0 = T1 = W;
+    }
+
+    // pass 2: chunked inclusive scan of tiles per sequence; each warp finds
+    // the sequence holding tile T0
+    bool found = T0 >= T1;
+    long long base = 0;
+    for (int c0 = 0; c0 < S; c0 += WARPS * 32) {
+        const int s = c0 + threadIdx.x;
+        long long v = s < S ? unit_tiles(clamp_len(a.context_lens, s, max_len)) : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long n = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += n;
+        }
+        if (lane == 31) s_wsum[warp] = v;
+        __syncthreads();
+        long long woff = base;
+        for (int i = 0; i < warp; ++i) woff += s_wsum[i];
+        s_scan[threadIdx.x] = v + woff;
+        __syncthreads();
+        const long long chunk_end = s_scan[WARPS * 32 - 1];
+        if (!found && T0 < chunk_end * Hkv) {
+            int hit_i = -1;
+            for (int i0 = 0; i0 < WARPS * 32 && hit_i < 0; i0 += 32) {
+                const unsigned m = __ballot_sync(0xffffffffu, s_scan[i0 + lane] * Hkv > T0);
+                if (m) hit_i = i0 + __ffs(m) - 1;
+            }
+            const long long excl = hit_i == 0 ? base : s_scan[hit_i - 1];
+            const long long nt = s_scan[hit_i] - excl;
+            const long long rem = T0 - excl * Hkv;
+            c.s = c0 + hit_i;
+            c.kvh = (int)(rem / nt);
+            c.j = (int)(rem % nt);
+            c.nt = (int)nt;
+            c.L = clamp_len(a.context_lens, c.s, max_len);
+            found = true;
+        }
+        base = chunk_end;
+        __syncthreads();
+    }
+}
+
+// CUDA-core decode worker: lane l owns head dims [4l, 4l + 4) of every query
+// head of the group.
+template <int GP, int WARPS, int NSTAGE>
+__global__ void __launch_bounds__(WARPS * 32)
+decode_simt_kernel(const DecodeArgs a) {
+    using Lay = SimtLayout<GP, WARPS, NSTAGE>;
+    constexpr int HP = GP >= 2 ? GP / 2 : 1;     // query heads whose scores a lane holds
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *ring = smem + warp * Lay::kWarpBytes;
+    float *sp = reinterpret_cast<float *>(ring + NSTAGE * Lay::kStageBytes);   // p[16][GP]
+    float *sa = sp + 16 * GP;                                                    // alpha[GP]
+    float *sl = sa + GP;                                                         // l[GP]
+
+    const int max_len = (int)min((int64_t)a.max_blocks_per_seq << a.block_size_log2,
+                                 (int64_t)0x7fffffff);
+    int64_t W, T0, T1;
+    int p_eff;
+    Cursor cc{0, 0, 0, 1, 0};
+    plan_share<WARPS>(a, max_len, W, p_eff, T0, T1, cc);
+    const int w = blockIdx.x * WARPS + warp;
+    if (w >= a.num_workers) return;
+    if (T0 >= T1) {
+        if (lane == 0) a.tasks[w] = make_int4(-1, 0, 0, 0);
+        return;
+    }
+
+    const int g = a.group;
+    const int t_lane = lane >> 1;                       // token whose scores this lane holds
+    const int hb = GP >= 2 ? (lane & 1) * HP : 0;       // first head of those scores
+    const uint16_t *qg = static_cast<const uint16_t *>(a.q);
+    uint32_t *outg = static_cast<uint32_t *>(a.out);
+
+    // producer: runs NSTAGE - 1 tiles ahead of the consumer
+    Cursor pc = cc;
+    int64_t Tp = T0;
+    int p_bid = tile_block(pc, a);
+    int stage_p = 0;
+#pragma unroll
+    for (int i = 0; i < NSTAGE - 1; ++i) {
+        if (Tp < T1) {
+            issue_tile(pc, p_bid, ring + stage_p * Lay::kStageBytes, a, lane);
+            cursor_advance(pc, a, max_len);
+            ++Tp;
+            p_bid = Tp < T1 ? tile_block(pc, a) : 0;
+        }
+        cp_async_commit();
+        stage_p = stage_p + 1 == NSTAGE ? 0 : stage_p + 1;
+    }
+
+    float qf[GP][4], o[GP][4], m_run[HP], l_run[HP];
+    int stage_c = 0;
+    int piece = 0;              // index of the current piece within this share
+    bool fresh = true;          // next tile starts a piece
+    int64_t piece_T = T0;       // flat index of the piece's first tile
+    int piece_j0 = 0;
+    int4 task = make_int4(-1, 0, 0, 0);
+
+    for (int64_t T = T0; T < T1; ++T) {
+        if (Tp < T1) {
+            issue_tile(pc, p_bid, ring + stage_p * Lay::kStageBytes, a, lane);
+            cursor_advance(pc, a, max_len);
+            ++Tp;
+            p_bid = Tp < T1 ? tile_block(pc, a) : 0;
+        }
+        cp_async_commit();
+        stage_p = stage_p + 1 == NSTAGE ? 0 : stage_p + 1;
+
+        if (fresh) {
+            fresh = false;
+            piece_T = T;
+            piece_j0 = cc.j;
+            const uint16_t *qrow = qg + ((int64_t)cc.s * a.num_q_heads + (int64_t)cc.kvh * g) * kHeadDim;
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                uint2 u = make_uint2(0u, 0u);
+                if (h < g) u = __ldg(reinterpret_cast<const uint2 *>(qrow + h * kHeadDim) + lane);
+                qf[h][0] = bf16_lo(u.x) * a.scale_log2;
+                qf[h][1] = bf16_hi(u.x) * a.scale_log2;
+                qf[h][2] = bf16_lo(u.y) * a.scale_log2;
+                qf[h][3] = bf16_hi(u.y) * a.scale_log2;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[h][i] = 0.f;
+            }
+#pragma unroll
+            for (int c = 0; c < HP; ++c) {
+                m_run[c] = -INFINITY;
+                l_run[c] = 0.f;
+            }
+        }
+
+        cp_async_wait<NSTAGE - 1>();
+        __syncwarp();
+        const uint8_t *sk = ring + stage_c * Lay::kStageBytes;
+        const uint8_t *sv = sk + kTileBytes;
+        const int valid = tile_valid(cc);
+
+        // scores: 16 tokens x GP heads, partial over this lane's 4 dims
+        float part[16 * GP];
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(sk + t * kRowBytes + lane * 8);
+            const float k0 = bf16_lo(u.x), k1 = bf16_hi(u.x), k2 = bf16_lo(u.y), k3 = bf16_hi(u.y);
+#pragma unroll
+            for (int h = 0; h < GP; ++h)
+                part[t * GP + h] = fmaf(qf[h][3], k3, fmaf(qf[h][2], k2, fmaf(qf[h][1], k1, qf[h][0] * k0)));
+        }
+        butterfly_sum<16 * GP>(part, lane);
+
+        // online softmax for this lane's token and heads
+        const bool tok_ok = t_lane < valid;
+#pragma unroll
+        for (int c = 0; c < HP; ++c) {
+            const float s = tok_ok ? part[c] : -INFINITY;
+            float mx = s;
+#pragma unroll
+            for (int m = 2; m <= 16; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+            const float m_new = fmaxf(m_run[c], mx);
+            const float ms = m_new == -INFINITY ? 0.f : m_new;
+            const float alpha = ex2(m_run[c] - ms);
+            const float p = ex2(s - ms);
+            l_run[c] = fmaf(l_run[c], alpha, p);
+            m_run[c] = m_new;
+            sp[t_lane * GP + hb + c] = p;
+            if (t_lane == 0) sa[hb + c] = alpha;
+        }
+        __syncwarp();
+
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            const float al = sa[h];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[h][i] *= al;
+        }
+#pragma unroll
+        for (int t = 0; t < 16; ++t) {
+            const uint2 u = *reinterpret_cast<const uint2 *>(sv + t * kRowBytes + lane * 8);
+            const float v0 = bf16_lo(u.x), v1 = bf16_hi(u.x), v2 = bf16_lo(u.y), v3 = bf16_hi(u.y);
+#pragma unroll
+            for (int h = 0; h < GP; ++h) {
+                const float p = sp[t * GP + h];
+                o[h][0] = fmaf(p, v0, o[h][0]);
+                o[h][1] = fmaf(p, v1, o[h][1]);
+                o[h][2] = fmaf(p, v2, o[h][2]);
+                o[h][3] = fmaf(p, v3, o[h][3]);
+            }
+        }
+        __syncwarp();
+        stage_c = stage_c + 1 == NSTAGE ? 0 : stage_c + 1;
+
+        const bool unit_end = cc.j == cc.nt - 1;
+        if (unit_end || T == T1 - 1) {
+            float lt[HP];
+#pragma unroll
+            for (int c = 0; c < HP; ++c) {
+                float x = l_run[c];
+#pragma unroll
+                for (int m = 2; m <= 16; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
+                lt[c] = x;
+            }
+            if (piece_j0 == 0 && unit_end) {
+                // the whole unit is in this share: normalise and write bf16
+                if (t_lane == 0) {
+#pragma unroll
+                    for (int c = 0; c < HP; ++c) sl[hb + c] = lt[c];
+                }
+                __syncwarp();
+                uint32_t *orow = outg + (((int64_t)cc.s * a.num_q_heads + (int64_t)cc.kvh * g) * kHeadDim) / 2;
+#pragma unroll
+                for (int h = 0; h < GP; ++h) {
+                    if (h < g) {
+                        const float l = sl[h];
+                        const float inv = l > 0.f ? 1.f / l : 0.f;
+                        uint2 pk;
+                        pk.x = pack_bf16x2(o[h][0] * inv, o[h][1] * inv);
+                        pk.y = pack_bf16x2(o[h][2] * inv, o[h][3] * inv);
+                        reinterpret_cast<uint2 *>(orow + h * (kHeadDim / 2))[lane] = pk;
+                    }
+                }
+                __syncwarp();
+            } else {
+                // a piece of a unit that other shares continue
+                const int slot = 2 * w + (piece == 0 ? 0 : 1);
+                float *po = a.part_o + (int64_t)slot * GP * kHeadDim;
+#pragma unroll
+                for (int h = 0; h < GP; ++h)
+                    reinterpret_cast<float4 *>(po + h * kHeadDim)[lane] =
+                        make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
+                if (t_lane == 0) {
+#pragma unroll
+                    for (int c = 0; c < HP; ++c)
+                        reinterpret_cast<float2 *>(a.part_ml)[(int64_t)slot * GP + hb + c] =
+                            make_float2(m_run[c], lt[c]);
+                }
+                if (piece_j0 == 0) {
+                    // this share holds the unit's first tile: it owns the combine
+                    const int64_t unit_end_T = piece_T + cc.nt;
+                    const int w_last = (int)((unit_end_T * p_eff - 1) / W);
+                    task = make_int4(cc.s, cc.kvh, slot, w_last);
+                }
+            }
+            ++piece;
+            fresh = true;
+        }
+        cursor_advance(cc, a, max_len);
+    }
+    cp_async_wait<0>();
+    if (lane == 0) a.tasks[w] = task;
+}
+
+// Log-sum-exp merge of the pieces of each split unit. One warp per worker's
+// task; lane l handles dims [4l, 4l + 4) of each query head.
+template <int GP>
+__global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int w = blockIdx.x * 4 + warp;
+    if (w >= a.num_workers) return;
+    const int4 task = a.tasks[w];
+    if (task.x < 0) return;
+    const int n = 1 + task.w - w;
+    const int g = a.group;
+    const float2 *ml = reinterpret_cast<const float2 *>(a.part_ml);
+    uint32_t *orow = static_cast<uint32_t *>(a.out) +
+                     (((int64_t)task.x * a.num_q_heads + (int64_t)task.y * g) * kHeadDim) / 2;
+    for (int h = 0; h < g; ++h) {
+        float M = -INFINITY;
+        for (int i = 0; i < n; ++i) {
+            const int slot = i == 0 ? task.z : 2 * (w + i);
+            M = fmaxf(M, ml[(int64_t)slot * GP + h].x);
+        }
+        float L = 0.f, acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+        for (int i = 0; i < n; ++i) {
+            const int slot = i == 0 ? task.z : 2 * (w + i);
+            const float2 e = ml[(int64_t)slot * GP + h];
+            const float wt = ex2(e.x - M);
+            L = fmaf(wt, e.y, L);
+            const float4 po = reinterpret_cast<const float4 *>(a.part_o + ((int64_t)slot * GP + h) * kHeadDim)[lane];
+            acc0 = fmaf(wt, po.x, acc0);
+            acc1 = fmaf(wt, po.y, acc1);
+            acc2 = fmaf(wt, po.z, acc2);
+            acc3 = fmaf(wt, po.w, acc3);
+        }
+        const float inv = L > 0.f ? 1.f / L : 0.f;
+        uint2 pk;
+        pk.x = pack_bf16x2(acc0 * inv, acc1 * inv);
+        pk.y = pack_bf16x2(acc2 * inv, acc3 * inv);
+        reinterpret_cast<uint2 *>(orow + h * (kHeadDim / 2))[lane] = pk;
+    }
+}
+
+template <int GP>
+struct SimtKernel {
+    using Lay = SimtLayout<GP, kSimtWarps, kSimtStages>;
+    static void *fn() { return reinterpret_cast<void *>(&decode_simt_kernel<GP, kSimtWarps, kSimtStages>); }
+    static cudaError_t prepare() {
+        return cudaFuncSetAttribute(decode_simt_kernel<GP, kSimtWarps, kSimtStages>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kCtaBytes);
+    }
+    static int ctas_per_sm() {
+        if (prepare() != cudaSuccess) return 0;
+        int n = 0;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
+                &n, decode_simt_kernel<GP, kSimtWarps, kSimtStages>, kSimtWarps * 32,
+                Lay::kCtaBytes) != cudaSuccess)
+            return 0;
+        return n;
+    }
+    static cudaError_t launch(const DecodeArgs &a, cudaStream_t st) {
+        cudaError_t e = prepare();
+        if (e != cudaSuccess) return e;
+        const int grid = (a.num_workers + kSimtWarps - 1) / kSimtWarps;
+        decode_simt_kernel<GP, kSimtWarps, kSimtStages>
+            <<<grid, kSimtWarps * 32, Lay::kCtaBytes, st>>>(a);
+        e = cudaGetLastError();
+        if (e != cudaSuccess) return e;
+        combine_kernel<GP><<<(a.num_workers + 3) / 4, 128, 0, st>>>(a);
+        return cudaGetLastError();
+    }
+};
+
+}  // namespace
+
+int decode_group_pad(int group) {
+    if (group < 1) return 0;
+    int gp = 1;
+    while (gp < group) gp <<= 1;
+    return gp <= 8 ? gp : 0;
+}
+
+int decode_default_workers(int group_pad, int sm_count) {
+    int per_sm = 0;
+    switch (group_pad) {
+        case 1: per_sm = SimtKernel<1>::ctas_per_sm(); break;
+        case 2: per_sm = SimtKernel<2>::ctas_per_sm(); break;
+        case 4: per_sm = SimtKernel<4>::ctas_per_sm(); break;
+        case 8: per_sm = SimtKernel<8>::ctas_per_sm(); break;
+        default: return 0;
+    }
+    if (per_sm < 1) return 0;
+    return sm_count * per_sm * kSimtWarps;
+}
+
+size_t decode_workspace_bytes(int group_pad, int num_workers) {
+    const size_t P = (size_t)num_workers;
+    return 2 * P * group_pad * kHeadDim * sizeof(float)   // part_o
+           + 2 * P * group_pad * 2 * sizeof(float)         // part_ml
+           + P * sizeof(int4);                             // tasks
+}
+
+void decode_carve_workspace(DecodeArgs &a, void *workspace, int group_pad) {
+    const size_t P = (size_t)a.num_workers;
+    char *p = static_cast<char *>(workspace);
+    a.part_o = reinterpret_cast<float *>(p);
+    p += 2 * P * group_pad * kHeadDim * sizeof(float);
+    a.part_ml = reinterpret_cast<float *>(p);
+    p += 2 * P * group_pad * 2 * sizeof(float);
+    a.tasks = reinterpret_cast<int4 *>(p);
+}
+
+cudaError_t launch_decode(const DecodeArgs &a, int group_pad, cudaStream_t stream) {
+    switch (group_pad) {
+        case 1: return SimtKernel<1>::launch(a, stream);
+        case 2: return SimtKernel<2>::launch(a, stream);
+        case 4: return SimtKernel<4>::launch(a, stream);
+        case 8: return SimtKernel<8>::launch(a, stream);
+        default: return cudaErrorInvalidValue;
+    }
+}
+
+}  // namespace pa

@@ -1,0 +1,55 @@
+// Internal launchers behind the C ABI (not part of the public header).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda_runtime.h>
+
+namespace pa {
+
+constexpr int kHeadDimPublic = 128;   // head_dim the ABI accepts
+constexpr int kDefaultMinTiles = 4;   // automatic shares hold at least this many 16-token tiles
+
+// Everything one paged-decode launch needs. Pointers are device memory.
+struct DecodeArgs {
+    const void *q;              // bf16 [S, Hq, 128]
+    const void *k_cache;        // bf16 [NB, bs, Hkv, 128]
+    const void *v_cache;
+    const int32_t *block_tables;  // [S, max_blocks_per_seq]
+    const int32_t *context_lens;  // [S]
+    void *out;                  // bf16 [S, Hq, 128]
+    float *part_o;              // [2P, GP, 128] unnormalised partial outputs
+    float *part_ml;             // [2P, GP, 2]   (running max in log2 units, sum)
+    int4 *tasks;                // [P] combine task of each worker
+    int num_seqs;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;                  // Hq / Hkv
+    int block_size_log2;
+    int max_blocks_per_seq;
+    int64_t num_blocks;
+    float scale_log2;           // scale * log2(e)
+    int num_workers;            // P: contiguous shares of the tile space
+    int min_tiles;              // fewest tiles a share may hold (1 = exactly P shares)
+};
+
+// Padded group size the kernels are instantiated for (power of two >= group),
+// or 0 when unsupported.
+int decode_group_pad(int group);
+
+// Workers (shares) per device when the caller does not force a count.
+int decode_default_workers(int group_pad, int sm_count);
+
+// Workspace bytes for P workers at padded group size GP.
+size_t decode_workspace_bytes(int group_pad, int num_workers);
+
+// Carve the workspace into DecodeArgs' part_o / part_ml / tasks.
+void decode_carve_workspace(DecodeArgs &a, void *workspace, int group_pad);
+
+cudaError_t launch_decode(const DecodeArgs &a, int group_pad, cudaStream_t stream);
+
+cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
+                                 const int64_t *slot_mapping, int64_t num_tokens, int row_elems,
+                                 int64_t num_slots, int sm_count, cudaStream_t stream);
+
+}  // namespace pa

@@ -1,0 +1,60 @@
+// store_kvcache: scatter new K/V rows into the paged cache through slot_mapping.
+//
+// Write side of the paged KV cache ("A vLLM engine small enough to read in one
+// sitting", paged KV cache management): row i of k/v goes to cache slot
+// slot_mapping[i] = block * block_size + offset, where block comes from the
+// sequence's block_table ("Building a minimal vLLM implementation",
+// sequence.py). One warp copies one row of num_kv_heads * head_dim bf16 for K
+// and the same for V with 16-byte loads and stores; -1 rows are skipped.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace pa {
+
+namespace {
+
+constexpr int kStoreWarps = 8;
+
+__global__ void __launch_bounds__(kStoreWarps * 32)
+store_kvcache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
+                     uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
+                     const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
+                     int row_chunks, int64_t num_slots) {
+    const int lane = threadIdx.x & 31;
+    const int64_t first = (int64_t)blockIdx.x * kStoreWarps + (threadIdx.x >> 5);
+    const int64_t stride = (int64_t)gridDim.x * kStoreWarps;
+    for (int64_t i = first; i < num_tokens; i += stride) {
+        const int64_t slot = slot_mapping[i];
+        if (slot < 0 || slot >= num_slots) continue;   // -1 padding, or out of range
+        const uint4 *ks = k + i * row_chunks;
+        const uint4 *vs = v + i * row_chunks;
+        uint4 *kd = k_cache + slot * row_chunks;
+        uint4 *vd = v_cache + slot * row_chunks;
+        for (int c = lane; c < row_chunks; c += 32) {
+            const uint4 a = __ldg(ks + c);
+            const uint4 b = __ldg(vs + c);
+            kd[c] = a;
+            vd[c] = b;
+        }
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
+                                 const int64_t *slot_mapping, int64_t num_tokens,
+                                 int row_elems, int64_t num_slots, int sm_count,
+                                 cudaStream_t stream) {
+    if (num_tokens == 0) return cudaSuccess;
+    const int row_chunks = row_elems / 8;   // 16-byte chunks per row
+    int64_t blocks = (num_tokens + kStoreWarps - 1) / kStoreWarps;
+    const int64_t cap = (int64_t)sm_count * 16;
+    if (blocks > cap) blocks = cap;
+    store_kvcache_kernel<<<(unsigned)blocks, kStoreWarps * 32, 0, stream>>>(
+        static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
+        static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_tokens,
+        row_chunks, num_slots);
+    return cudaGetLastError();
+}
+
+}  // namespace pa

@@ -1,0 +1,176 @@
+"""Python binding of libpagedattn (ctypes): argument marshalling only.
+
+Every function here checks tensor devices, dtypes and shapes, then calls the
+C ABI declared in ``include/pagedattn.h`` with raw device pointers and the
+current torch CUDA stream. All computation happens in the library's CUDA
+kernels; there is no fallback. If the shared library has not been built, the
+first call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+PA_OK, PA_ERR_INVALID_ARG, PA_ERR_UNSUPPORTED, PA_ERR_WORKSPACE, PA_ERR_CUDA = range(5)
+
+# every entry point include/pagedattn.h declares, with its ctypes signature
+_P, _I32, _I64, _F32, _SZ = (ctypes.c_void_p, ctypes.c_int, ctypes.c_int64, ctypes.c_float,
+                             ctypes.c_size_t)
+SIGNATURES = {
+    "pa_status_string": ([_I32], ctypes.c_char_p),
+    "pa_store_kvcache": ([_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64, _P], _I32),
+    "pa_decode_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
+    "pa_decode": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32, _I64,
+                   _P, _SZ, _P], _I32),
+    "pa_decode_splitk": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32,
+                          _I64, _P, _SZ, _I32, _P], _I32),
+}
+
+_lock = threading.Lock()
+_lib = None
+_workspaces = {}
+
+
+class PagedAttnError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        self.status = status
+        super().__init__(f"{fn} failed: {status_string(status)} ({status})")
+
+
+def library_path() -> str:
+    return _build.LIB_PATH
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded libpagedattn; raises if it has not been built."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB_PATH
+            if not os.path.exists(path):
+                raise RuntimeError(
+                    f"libpagedattn is not built ({path} missing): run "
+                    "paged_kv_cache_255_gb300.build.build() first")
+            handle = ctypes.CDLL(path)
+            for name, (args, res) in SIGNATURES.items():
+                fn = getattr(handle, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = handle
+    return _lib
+
+
+def status_string(status: int) -> str:
+    return lib().pa_status_string(int(status)).decode()
+
+
+def _check(fn: str, status: int):
+    if status != PA_OK:
+        raise PagedAttnError(fn, status)
+
+
+def _stream_ptr(stream, device) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream(device)
+    return int(stream.cuda_stream)
+
+
+def _cuda(t: torch.Tensor, name: str, dtype, device=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if device is not None and t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device}")
+
+
+def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):
+    """Write row i of k/v to cache slot slot_mapping[i] (-1 rows skipped).
+
+    k, v: bf16 [N, Hkv, D]; k_cache, v_cache: bf16 [NB, bs, Hkv, D];
+    slot_mapping: int64 [N]. Runs on the current stream (or ``stream``).
+    """
+    dev = k_cache.device
+    for t, n, dt in ((k, "k", torch.bfloat16), (v, "v", torch.bfloat16),
+                     (k_cache, "k_cache", torch.bfloat16), (v_cache, "v_cache", torch.bfloat16),
+                     (slot_mapping, "slot_mapping", torch.int64)):
+        _cuda(t, n, dt, dev)
+    NB, bs, Hkv, D = k_cache.shape
+    N = slot_mapping.shape[0]
+    if v_cache.shape != k_cache.shape or k.shape != (N, Hkv, D) or v.shape != (N, Hkv, D):
+        raise ValueError("shape mismatch between k, v, caches and slot_mapping")
+    with torch.cuda.device(dev):
+        st = lib().pa_store_kvcache(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(),
+                                    v_cache.data_ptr(), slot_mapping.data_ptr(), N, Hkv, D, bs,
+                                    NB, _stream_ptr(stream, dev))
+    _check("pa_store_kvcache", st)
+
+
+def decode_workspace_size(num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
+                          num_partitions: int = 0, device=None) -> int:
+    """Workspace bytes pa_decode needs on ``device`` (default: current)."""
+    with torch.cuda.device(device if device is not None else torch.cuda.current_device()):
+        n = lib().pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim, num_partitions)
+    if n == 0:
+        raise ValueError("unsupported head configuration")
+    return int(n)
+
+
+def workspace_for(num_q_heads, num_kv_heads, head_dim=128, num_partitions=0, device=None):
+    """A cached uint8 workspace tensor big enough for these heads on ``device``."""
+    device = torch.device(device if device is not None else f"cuda:{torch.cuda.current_device()}")
+    n = decode_workspace_size(num_q_heads, num_kv_heads, head_dim, num_partitions, device)
+    key = (device, n)
+    ws = _workspaces.get(key)
+    if ws is None:
+        ws = torch.empty(n, dtype=torch.uint8, device=device)
+        _workspaces[key] = ws
+    return ws
+
+
+def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, workspace=None,
+           num_partitions: int = 0, stream=None):
+    """Single-token paged decode attention; returns ``out`` (bf16 [S, Hq, D]).
+
+    q: bf16 [S, Hq, D]; caches: bf16 [NB, bs, Hkv, D]; block_tables: int32
+    [S, max_blocks]; context_lens: int32 [S]. ``num_partitions`` > 0 forces
+    the split-K share count (pa_decode_splitk).
+    """
+    dev = q.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                     (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
+                     (context_lens, "context_lens", torch.int32)):
+        _cuda(t, n, dt, dev)
+    S, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or block_tables.dim() != 2 \
+            or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("shape mismatch between q, caches, block_tables and context_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda(out, "out", torch.bfloat16, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = workspace_for(Hq, Hkv, D, num_partitions, dev)
+    else:
+        _cuda(workspace, "workspace", workspace.dtype, dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    args = (q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+            block_tables.shape[1], context_lens.data_ptr(), float(scale), out.data_ptr(), S, Hq,
+            Hkv, D, bs, NB, workspace.data_ptr(), ws_bytes)
+    with torch.cuda.device(dev):
+        if num_partitions:
+            st = lib().pa_decode_splitk(*args, int(num_partitions), _stream_ptr(stream, dev))
+        else:
+            st = lib().pa_decode(*args, _stream_ptr(stream, dev))
+    _check("pa_decode", st)
+    return out

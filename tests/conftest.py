@@ -20,3 +20,11 @@ def pytest_collection_modifyitems(config, items):
     for item in items:
         if "gpu" in item.keywords:
             item.add_marker(skip)
+
+
+@pytest.fixture(scope="session")
+def pa_lib():
+    """libpagedattn built in-tree (nvcc cross-compiles without a GPU) and loaded."""
+    from paged_kv_cache_255_gb300 import build, pagedattn
+    build.build()
+    return pagedattn.lib()
