@@ -92,7 +92,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu=timestamp,{','.join(self.FIELDS)}",
-                 "--format=csv,noheader,nounits", "-lms", "100", "-i", str(index)],
+                 "--format=csv,noheader,nounits", "-lms", "20", "-i", str(index)],
                 stdout=self.fh, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -350,8 +350,8 @@ def run_gpu(args, rank, world, local):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=50)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.SPECS))
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="run a copy of the workload with this many sequences (profiling)")

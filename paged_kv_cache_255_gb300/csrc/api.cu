@@ -2,6 +2,8 @@
 // The public contract is in include/pagedattn.h.
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
+#include <cstring>
 
 #include "../../include/pagedattn.h"
 #include "kernels.h"
@@ -25,11 +27,20 @@ int current_sm_count() {
     return n;
 }
 
+// Tile computation for decode: tensor cores unless PA_DECODE_KERNEL=simt asks
+// for the CUDA-core variant (kept for comparison and testing). Group sizes
+// above 8 always use the tensor cores.
+pa::DecodeKernel decode_kernel_choice(int group_pad) {
+    const char *e = std::getenv("PA_DECODE_KERNEL");
+    if (e && std::strcmp(e, "simt") == 0 && group_pad <= 8) return pa::DecodeKernel::kSimt;
+    return pa::DecodeKernel::kMma;
+}
+
 // Shares of the tile space for a call: forced, or from the device.
-int plan_workers(int group_pad, int num_partitions) {
+int plan_workers(int group_pad, pa::DecodeKernel k, int num_partitions) {
     if (num_partitions > 0) return num_partitions;
     const int sms = current_sm_count();
-    return sms > 0 ? pa::decode_default_workers(group_pad, sms) : 0;
+    return sms > 0 ? pa::decode_default_workers(group_pad, k, sms) : 0;
 }
 
 pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
@@ -53,7 +64,8 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
         return PA_ERR_INVALID_ARG;
     if (max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_INVALID_ARG;
 
-    const int P = plan_workers(gp, num_partitions);
+    const pa::DecodeKernel kind = decode_kernel_choice(gp);
+    const int P = plan_workers(gp, kind, num_partitions);
     if (P <= 0) return PA_ERR_CUDA;
     if (!workspace || !aligned16(workspace) || workspace_bytes < pa::decode_workspace_bytes(gp, P))
         return PA_ERR_WORKSPACE;
@@ -76,7 +88,7 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
     a.num_workers = P;
     a.min_tiles = num_partitions > 0 ? 1 : pa::kDefaultMinTiles;
     pa::decode_carve_workspace(a, workspace, gp);
-    const cudaError_t e = pa::launch_decode(a, gp, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = pa::launch_decode(a, gp, kind, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
@@ -119,7 +131,12 @@ size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
         return 0;
     const int gp = pa::decode_group_pad(num_q_heads / num_kv_heads);
     if (gp == 0) return 0;
-    const int P = plan_workers(gp, num_partitions);
+    // sized for the larger of the two variants' default share counts
+    int P = plan_workers(gp, pa::DecodeKernel::kMma, num_partitions);
+    if (num_partitions == 0 && gp <= 8) {
+        const int Ps = plan_workers(gp, pa::DecodeKernel::kSimt, 0);
+        P = Ps > P ? Ps : P;
+    }
     if (P <= 0) return 0;
     return pa::decode_workspace_bytes(gp, P);
 }

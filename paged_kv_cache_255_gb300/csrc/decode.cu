@@ -17,14 +17,19 @@
 //     every SM streams the same number of bytes whatever the length mix.
 //   * A worker streams its tiles through a private NSTAGE-deep cp.async ring
 //     in shared memory (16-byte zero-filling copies; rows past the sequence
-//     end are never read), computes q.K for all g query heads of the KV head
-//     in fp32, keeps an online softmax (running max in log2 units, running
-//     sum) and accumulates P.V in fp32.
+//     end are never read) and keeps, per query head of its KV head's group, an
+//     online softmax (running max in log2 units, running sum) and an fp32
+//     accumulator of P.V.
 //   * A unit that lies wholly in one share is written straight to `out`. A
 //     unit cut by share boundaries leaves one partial (o, m, l) per share in
 //     the workspace; the worker holding its first tile records a combine task,
 //     and the combine kernel merges the pieces by log-sum-exp weights
 //     (split-K / flash-decoding).
+// Two interchangeable tile computations sit inside the same worker loop:
+//   * MmaTile: q.K^T and P.V on the tensor cores with mma.sync m16n8k16 bf16
+//     (fp32 accumulate): 16 tokens x 8 (or 16) query heads x 128 dims per
+//     tile; the default.
+//   * SimtTile: the same on the CUDA cores, lane l owning dims [4l, 4l + 4).
 // The kernels never wait on one another inside a launch.
 #include <cmath>
 
@@ -35,8 +40,10 @@ namespace pa {
 
 namespace {
 
-constexpr int kSimtWarps = 4;      // workers per CTA
-constexpr int kSimtStages = 3;     // tiles in flight per worker (ring depth)
+constexpr int kWarps = 4;      // workers per CTA
+constexpr int kStages = 3;     // tiles in flight per worker (ring depth)
+constexpr int kStageBytes = 2 * kTileBytes;   // K tile then V tile
+constexpr float kNegInf = -INFINITY;
 
 __device__ __forceinline__ int clamp_len(const int32_t *cl, int s, int max_len) {
     int L = __ldg(cl + s);
@@ -79,8 +86,12 @@ __device__ __forceinline__ int tile_block(const Cursor &c, const DecodeArgs &a) 
 }
 
 // Issue the cp.async copies of one K tile and one V tile (16 rows x 256 B
-// each) into `stage`. Lane l copies 16-byte column (l & 15) of rows
-// (l >> 4) + 2i; each instruction covers two whole 256-byte rows.
+// each) into `stage`. Lane l copies 16-byte chunk (l & 15) of rows
+// (l >> 4) + 2i; each instruction covers two whole 256-byte rows. With
+// SWZ the chunk lands at position chunk ^ (row & 7) of its row, so that the
+// eight rows an ldmatrix reads at one logical chunk fall in eight different
+// bank groups.
+template <bool SWZ>
 __device__ __forceinline__ void issue_tile(const Cursor &c, int bid, uint8_t *stage,
                                            const DecodeArgs &a, int lane) {
     int valid = tile_valid(c);
@@ -90,24 +101,187 @@ __device__ __forceinline__ void issue_tile(const Cursor &c, int bid, uint8_t *st
     const int64_t rstride = (int64_t)a.num_kv_heads * kRowBytes;
     const char *kb = static_cast<const char *>(a.k_cache) + row0 * kRowBytes;
     const char *vb = static_cast<const char *>(a.v_cache) + row0 * kRowBytes;
-    const int col = (lane & 15) * 16;
+    const int chunk = lane & 15;
     const uint32_t dst = smem_u32(stage);
 #pragma unroll
     for (int i = 0; i < 8; ++i) {
         const int r = (lane >> 4) + 2 * i;
         const bool ok = r < valid;
-        const int64_t o = ok ? r * rstride + col : 0;
-        cp_async_16(dst + r * kRowBytes + col, ok ? kb + o : static_cast<const char *>(a.k_cache),
-                    ok ? 16 : 0);
-        cp_async_16(dst + kTileBytes + r * kRowBytes + col,
+        const int64_t o = ok ? r * rstride + chunk * 16 : 0;
+        const int pos = SWZ ? (chunk ^ (r & 7)) : chunk;
+        cp_async_16(dst + r * kRowBytes + pos * 16,
+                    ok ? kb + o : static_cast<const char *>(a.k_cache), ok ? 16 : 0);
+        cp_async_16(dst + kTileBytes + r * kRowBytes + pos * 16,
                     ok ? vb + o : static_cast<const char *>(a.v_cache), ok ? 16 : 0);
     }
 }
 
+// ---------------------------------------------------------------------------
+// Tile computation on the tensor cores.
+//
+// Scores as S^T = K Q^T: A = the K tile (16 tokens x 16 dims per k-step,
+// ldmatrix from the swizzled ring), B = Q^T (16 dims x 8 heads, kept in
+// registers for the unit), C = 16 tokens x 8 heads in fp32. Lane (gid =
+// lane / 4, tig = lane % 4) holds tokens gid and gid + 8 of heads 2 tig and
+// 2 tig + 1, so the per-head max over tokens is a 3-step xor reduction.
+// P^T (bf16) becomes the B operand of O^T += V^T P^T through one movmatrix
+// transpose per 8x8 half; A = V^T comes from the V tile by ldmatrix.trans.
+// O^T (128 dims x 8 heads, fp32) lives in 8 m-tiles of 4 registers.
+template <int GP>
+struct MmaTile {
+    static constexpr int NT = GP > 8 ? 2 : 1;      // 8-head column tiles
+    static constexpr bool kSwizzle = true;
+    static constexpr int kScratchFloats = 0;
+    uint32_t qb[NT][8][2];
+    float o[NT][8][4];
+    float m[NT][2], l[NT][2];
+
+    __device__ __forceinline__ void begin(const uint16_t *qrow, int g, int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const int h = nt * 8 + gid;
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk) {
+                uint32_t w0 = 0u, w1 = 0u;
+                if (h < g) {
+                    const uint32_t *p = reinterpret_cast<const uint32_t *>(qrow + h * kHeadDim + kk * 16 + tig * 2);
+                    w0 = __ldg(p);
+                    w1 = __ldg(p + 4);
+                }
+                qb[nt][kk][0] = w0;
+                qb[nt][kk][1] = w1;
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+                for (int i = 0; i < 4; ++i) o[nt][mt][i] = 0.f;
+            m[nt][0] = m[nt][1] = kNegInf;
+            l[nt][0] = l[nt][1] = 0.f;
+        }
+    }
+
+    __device__ __forceinline__ void tile(const uint8_t *stage, int valid, float scale_log2,
+                                         float *, int lane) {
+        const uint32_t base = smem_u32(stage);
+        const int i7 = lane & 7, mi = lane >> 3;
+        const int gid = lane >> 2, tig = lane & 3;
+
+        float s[NT][4];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
+        const uint32_t krow = base + (i7 + 8 * (mi & 1)) * kRowBytes;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t a[4];
+            ldmatrix_x4(krow + (((2 * kk + (mi >> 1)) ^ i7) << 4), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(s[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
+        }
+
+        const bool ok0 = gid < valid, ok1 = gid + 8 < valid;
+        uint32_t pb0[NT], pb1[NT];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            const float s0 = ok0 ? s[nt][0] * scale_log2 : kNegInf;
+            const float s1 = ok0 ? s[nt][1] * scale_log2 : kNegInf;
+            const float s2 = ok1 ? s[nt][2] * scale_log2 : kNegInf;
+            const float s3 = ok1 ? s[nt][3] * scale_log2 : kNegInf;
+            float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
+#pragma unroll
+            for (int x = 4; x <= 16; x <<= 1) {
+                mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, x));
+                mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, x));
+            }
+            const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
+            const float ms0 = mn0 == kNegInf ? 0.f : mn0, ms1 = mn1 == kNegInf ? 0.f : mn1;
+            const float al0 = ex2(m[nt][0] - ms0), al1 = ex2(m[nt][1] - ms1);
+            const uint32_t w0 = pack_bf16x2(ex2(s0 - ms0), ex2(s1 - ms1));   // token gid
+            const uint32_t w1 = pack_bf16x2(ex2(s2 - ms0), ex2(s3 - ms1));   // token gid + 8
+            // the running sum adds the same bf16-rounded weights the tensor cores use
+            l[nt][0] = fmaf(l[nt][0], al0, bf16_lo(w0) + bf16_lo(w1));
+            l[nt][1] = fmaf(l[nt][1], al1, bf16_hi(w0) + bf16_hi(w1));
+            m[nt][0] = mn0;
+            m[nt][1] = mn1;
+            pb0[nt] = movmatrix_trans(w0);
+            pb1[nt] = movmatrix_trans(w1);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                o[nt][mt][0] *= al0;
+                o[nt][mt][1] *= al1;
+                o[nt][mt][2] *= al0;
+                o[nt][mt][3] *= al1;
+            }
+        }
+
+        const uint32_t vrow = base + kTileBytes + (i7 + 8 * (mi >> 1)) * kRowBytes;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            uint32_t a[4];
+            ldmatrix_x4_trans(vrow + (((2 * mt + (mi & 1)) ^ i7) << 4), a);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a, pb0[nt], pb1[nt]);
+        }
+    }
+
+    // Leave o[h][4 lane .. 4 lane + 3] (unnormalised) in `oc`, and the per-head
+    // running max and total sum in sm_m / sm_l. `scr` is a free 8 KB stage.
+    __device__ __forceinline__ void finish(float *scr, float *sm_m, float *sm_l, float (&oc)[GP][4],
+                                           int lane) {
+        const int gid = lane >> 2, tig = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+            float lt0 = l[nt][0], lt1 = l[nt][1];
+#pragma unroll
+            for (int x = 4; x <= 16; x <<= 1) {
+                lt0 += __shfl_xor_sync(0xffffffffu, lt0, x);
+                lt1 += __shfl_xor_sync(0xffffffffu, lt1, x);
+            }
+            const int h0 = nt * 8 + 2 * tig;
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const int d0 = mt * 16 + gid;
+                if (h0 < GP) {
+                    scr[h0 * kHeadDim + d0] = o[nt][mt][0];
+                    scr[h0 * kHeadDim + d0 + 8] = o[nt][mt][2];
+                }
+                if (h0 + 1 < GP) {
+                    scr[(h0 + 1) * kHeadDim + d0] = o[nt][mt][1];
+                    scr[(h0 + 1) * kHeadDim + d0 + 8] = o[nt][mt][3];
+                }
+            }
+            if (gid == 0) {
+                if (h0 < GP) {
+                    sm_m[h0] = m[nt][0];
+                    sm_l[h0] = lt0;
+                }
+                if (h0 + 1 < GP) {
+                    sm_m[h0 + 1] = m[nt][1];
+                    sm_l[h0 + 1] = lt1;
+                }
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            const float4 v = reinterpret_cast<const float4 *>(scr + h * kHeadDim)[lane];
+            oc[h][0] = v.x;
+            oc[h][1] = v.y;
+            oc[h][2] = v.z;
+            oc[h][3] = v.w;
+        }
+    }
+};
+
+// ---------------------------------------------------------------------------
+// Tile computation on the CUDA cores: lane l owns head dims [4l, 4l + 4) of
+// every query head of the group.
+
 // Sum NV per-lane values across the 32 lanes, halving the set at each of the
 // five xor steps: afterwards lane l holds max(1, NV / 32) fully reduced
-// values, originally at indices (l >> (5 - log2 NV)) ... for NV < 32 and
-// l * NV / 32 + i for NV >= 32.
+// values, originally at indices l * NV / 32 + i (NV >= 32) or l >> 1 (NV = 16).
 template <int NV>
 __device__ __forceinline__ void butterfly_sum(float (&v)[NV], int lane) {
 #pragma unroll
@@ -128,188 +302,42 @@ __device__ __forceinline__ void butterfly_sum(float (&v)[NV], int lane) {
     }
 }
 
-template <int GP, int WARPS, int NSTAGE>
-struct SimtLayout {
-    static constexpr int kStageBytes = 2 * kTileBytes;               // K tile then V tile
-    static constexpr int kScratchFloats = 16 * GP + 2 * GP;          // p[16][GP], alpha, l
-    static constexpr int kScratchBytes = ((kScratchFloats * 4 + 127) / 128) * 128;
-    static constexpr int kWarpBytes = NSTAGE * kStageBytes + kScratchBytes;
-    static constexpr int kCtaBytes = WARPS * kWarpBytes;
-};
-
-// CTA prologue shared by the decode kernels: the total tile count W and the
-// position (sequence, KV head, tile) of this warp's first tile.
-template <int WARPS>
-__device__ __forceinline__ void plan_share(const DecodeArgs &a, int max_len, int64_t &W,
-                                           int &p_eff, int64_t &T0, int64_t &T1, Cursor &c) {
-    __shared__ long long s_wsum[WARPS];
-    __shared__ long long s_scan[WARPS * 32];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int S = a.num_seqs, Hkv = a.num_kv_heads;
-
-    // pass 1: total tiles
-    long long local = 0;
-    for (int s = threadIdx.x; s < S; s += WARPS * 32) local += unit_tiles(clamp_len(a.context_lens, s, max_len));
-#pragma unroll
-    for (int m = 16; m >= 1; m >>= 1) local += __shfl_xor_sync(0xffffffffu, local, m);
-    if (lane == 0) s_wsum[warp] = local;
-    __syncthreads();
-    long long total = 0;
-#pragma unroll
-    for (int i = 0; i < WARPS; ++i) total += s_wsum[i];
-    __syncthreads();
-    W = total * Hkv;
-
-    int64_t pe = W / (a.min_tiles > 0 ? a.min_tiles : 1);
-    if (pe < 1) pe = 1;
-    if (pe > a.num_workers) pe = a.num_workers;
-    p_eff = (int)pe;
-    const int w = blockIdx.x * WARPS + warp;
-    if (w < p_eff) {
-        T0 = (int64_t)w * W / p_eff;
-        T1 = (int64_t)(w + 1) * W / p_eff;
-    } else {
-        T0 = T1 = W;
-    }
-
-    // pass 2: chunked inclusive scan of tiles per sequence; each warp finds
-    // the sequence holding tile T0
-    bool found = T0 >= T1;
-    long long base = 0;
-    for (int c0 = 0; c0 < S; c0 += WARPS * 32) {
-        const int s = c0 + threadIdx.x;
-        long long v = s < S ? unit_tiles(clamp_len(a.context_lens, s, max_len)) : 0;
-#pragma unroll
-        for (int off = 1; off < 32; off <<= 1) {
-            const long long n = __shfl_up_sync(0xffffffffu, v, off);
-            if (lane >= off) v += n;
-        }
-        if (lane == 31) s_wsum[warp] = v;
-        __syncthreads();
-        long long woff = base;
-        for (int i = 0; i < warp; ++i) woff += s_wsum[i];
-        s_scan[threadIdx.x] = v + woff;
-        __syncthreads();
-        const long long chunk_end = s_scan[WARPS * 32 - 1];
-        if (!found && T0 < chunk_end * Hkv) {
-            int hit_i = -1;
-            for (int i0 = 0; i0 < WARPS * 32 && hit_i < 0; i0 += 32) {
-                const unsigned m = __ballot_sync(0xffffffffu, s_scan[i0 + lane] * Hkv > T0);
-                if (m) hit_i = i0 + __ffs(m) - 1;
-            }
-            const long long excl = hit_i == 0 ? base : s_scan[hit_i - 1];
-            const long long nt = s_scan[hit_i] - excl;
-            const long long rem = T0 - excl * Hkv;
-            c.s = c0 + hit_i;
-            c.kvh = (int)(rem / nt);
-            c.j = (int)(rem % nt);
-            c.nt = (int)nt;
-            c.L = clamp_len(a.context_lens, c.s, max_len);
-            found = true;
-        }
-        base = chunk_end;
-        __syncthreads();
-    }
-}
-
-// CUDA-core decode worker: lane l owns head dims [4l, 4l + 4) of every query
-// head of the group.
-template <int GP, int WARPS, int NSTAGE>
-__global__ void __launch_bounds__(WARPS * 32)
-decode_simt_kernel(const DecodeArgs a) {
-    using Lay = SimtLayout<GP, WARPS, NSTAGE>;
-    constexpr int HP = GP >= 2 ? GP / 2 : 1;     // query heads whose scores a lane holds
-    extern __shared__ __align__(128) uint8_t smem[];
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *ring = smem + warp * Lay::kWarpBytes;
-    float *sp = reinterpret_cast<float *>(ring + NSTAGE * Lay::kStageBytes);   // p[16][GP]
-    float *sa = sp + 16 * GP;                                                    // alpha[GP]
-    float *sl = sa + GP;                                                         // l[GP]
-
-    const int max_len = (int)min((int64_t)a.max_blocks_per_seq << a.block_size_log2,
-                                 (int64_t)0x7fffffff);
-    int64_t W, T0, T1;
-    int p_eff;
-    Cursor cc{0, 0, 0, 1, 0};
-    plan_share<WARPS>(a, max_len, W, p_eff, T0, T1, cc);
-    const int w = blockIdx.x * WARPS + warp;
-    if (w >= a.num_workers) return;
-    if (T0 >= T1) {
-        if (lane == 0) a.tasks[w] = make_int4(-1, 0, 0, 0);
-        return;
-    }
-
-    const int g = a.group;
-    const int t_lane = lane >> 1;                       // token whose scores this lane holds
-    const int hb = GP >= 2 ? (lane & 1) * HP : 0;       // first head of those scores
-    const uint16_t *qg = static_cast<const uint16_t *>(a.q);
-    uint32_t *outg = static_cast<uint32_t *>(a.out);
-
-    // producer: runs NSTAGE - 1 tiles ahead of the consumer
-    Cursor pc = cc;
-    int64_t Tp = T0;
-    int p_bid = tile_block(pc, a);
-    int stage_p = 0;
-#pragma unroll
-    for (int i = 0; i < NSTAGE - 1; ++i) {
-        if (Tp < T1) {
-            issue_tile(pc, p_bid, ring + stage_p * Lay::kStageBytes, a, lane);
-            cursor_advance(pc, a, max_len);
-            ++Tp;
-            p_bid = Tp < T1 ? tile_block(pc, a) : 0;
-        }
-        cp_async_commit();
-        stage_p = stage_p + 1 == NSTAGE ? 0 : stage_p + 1;
-    }
-
+template <int GP>
+struct SimtTile {
+    static constexpr int HP = GP >= 2 ? GP / 2 : 1;     // heads whose scores a lane holds
+    static constexpr bool kSwizzle = false;
+    static constexpr int kScratchFloats = 16 * GP + GP;  // p[16][GP], alpha[GP]
     float qf[GP][4], o[GP][4], m_run[HP], l_run[HP];
-    int stage_c = 0;
-    int piece = 0;              // index of the current piece within this share
-    bool fresh = true;          // next tile starts a piece
-    int64_t piece_T = T0;       // flat index of the piece's first tile
-    int piece_j0 = 0;
-    int4 task = make_int4(-1, 0, 0, 0);
+    float scale_log2_;
 
-    for (int64_t T = T0; T < T1; ++T) {
-        if (Tp < T1) {
-            issue_tile(pc, p_bid, ring + stage_p * Lay::kStageBytes, a, lane);
-            cursor_advance(pc, a, max_len);
-            ++Tp;
-            p_bid = Tp < T1 ? tile_block(pc, a) : 0;
+    __device__ __forceinline__ void begin(const uint16_t *qrow, int g, int lane) {
+#pragma unroll
+        for (int h = 0; h < GP; ++h) {
+            uint2 u = make_uint2(0u, 0u);
+            if (h < g) u = __ldg(reinterpret_cast<const uint2 *>(qrow + h * kHeadDim) + lane);
+            qf[h][0] = bf16_lo(u.x);
+            qf[h][1] = bf16_hi(u.x);
+            qf[h][2] = bf16_lo(u.y);
+            qf[h][3] = bf16_hi(u.y);
+#pragma unroll
+            for (int i = 0; i < 4; ++i) o[h][i] = 0.f;
         }
-        cp_async_commit();
-        stage_p = stage_p + 1 == NSTAGE ? 0 : stage_p + 1;
-
-        if (fresh) {
-            fresh = false;
-            piece_T = T;
-            piece_j0 = cc.j;
-            const uint16_t *qrow = qg + ((int64_t)cc.s * a.num_q_heads + (int64_t)cc.kvh * g) * kHeadDim;
 #pragma unroll
-            for (int h = 0; h < GP; ++h) {
-                uint2 u = make_uint2(0u, 0u);
-                if (h < g) u = __ldg(reinterpret_cast<const uint2 *>(qrow + h * kHeadDim) + lane);
-                qf[h][0] = bf16_lo(u.x) * a.scale_log2;
-                qf[h][1] = bf16_hi(u.x) * a.scale_log2;
-                qf[h][2] = bf16_lo(u.y) * a.scale_log2;
-                qf[h][3] = bf16_hi(u.y) * a.scale_log2;
-#pragma unroll
-                for (int i = 0; i < 4; ++i) o[h][i] = 0.f;
-            }
-#pragma unroll
-            for (int c = 0; c < HP; ++c) {
-                m_run[c] = -INFINITY;
-                l_run[c] = 0.f;
-            }
+        for (int c = 0; c < HP; ++c) {
+            m_run[c] = kNegInf;
+            l_run[c] = 0.f;
         }
+    }
 
-        cp_async_wait<NSTAGE - 1>();
-        __syncwarp();
-        const uint8_t *sk = ring + stage_c * Lay::kStageBytes;
-        const uint8_t *sv = sk + kTileBytes;
-        const int valid = tile_valid(cc);
+    __device__ __forceinline__ void tile(const uint8_t *stage, int valid, float scale_log2,
+                                         float *scratch, int lane) {
+        const uint8_t *sk = stage;
+        const uint8_t *sv = stage + kTileBytes;
+        float *sp = scratch;              // p[16][GP]
+        float *sa = scratch + 16 * GP;    // alpha[GP]
+        const int t_lane = lane >> 1;
+        const int hb = GP >= 2 ? (lane & 1) * HP : 0;
 
-        // scores: 16 tokens x GP heads, partial over this lane's 4 dims
         float part[16 * GP];
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
@@ -321,16 +349,15 @@ decode_simt_kernel(const DecodeArgs a) {
         }
         butterfly_sum<16 * GP>(part, lane);
 
-        // online softmax for this lane's token and heads
         const bool tok_ok = t_lane < valid;
 #pragma unroll
         for (int c = 0; c < HP; ++c) {
-            const float s = tok_ok ? part[c] : -INFINITY;
+            const float s = tok_ok ? part[c] * scale_log2 : kNegInf;
             float mx = s;
 #pragma unroll
-            for (int m = 2; m <= 16; m <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, m));
+            for (int x = 2; x <= 16; x <<= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, x));
             const float m_new = fmaxf(m_run[c], mx);
-            const float ms = m_new == -INFINITY ? 0.f : m_new;
+            const float ms = m_new == kNegInf ? 0.f : m_new;
             const float alpha = ex2(m_run[c] - ms);
             const float p = ex2(s - ms);
             l_run[c] = fmaf(l_run[c], alpha, p);
@@ -360,38 +387,211 @@ decode_simt_kernel(const DecodeArgs a) {
             }
         }
         __syncwarp();
-        stage_c = stage_c + 1 == NSTAGE ? 0 : stage_c + 1;
+    }
+
+    __device__ __forceinline__ void finish(float *, float *sm_m, float *sm_l, float (&oc)[GP][4],
+                                           int lane) {
+        const int t_lane = lane >> 1;
+        const int hb = GP >= 2 ? (lane & 1) * HP : 0;
+#pragma unroll
+        for (int c = 0; c < HP; ++c) {
+            float x = l_run[c];
+#pragma unroll
+            for (int msk = 2; msk <= 16; msk <<= 1) x += __shfl_xor_sync(0xffffffffu, x, msk);
+            if (t_lane == 0) {
+                sm_m[hb + c] = m_run[c];
+                sm_l[hb + c] = x;
+            }
+        }
+        __syncwarp();
+#pragma unroll
+        for (int h = 0; h < GP; ++h)
+#pragma unroll
+            for (int i = 0; i < 4; ++i) oc[h][i] = o[h][i];
+    }
+};
+
+// Per-warp shared memory: the ring, then the tile scratch, then m/l per head.
+template <class Tile, int GP>
+struct Layout {
+    static constexpr int kSmallFloats = Tile::kScratchFloats + 2 * GP;
+    static constexpr int kWarpBytes = kStages * kStageBytes + ((kSmallFloats * 4 + 127) / 128) * 128;
+    static constexpr int kCtaBytes = kWarps * kWarpBytes;
+};
+
+// CTA prologue: the total tile count W, the share count actually used, and
+// the position (sequence, KV head, tile) of this warp's first tile.
+__device__ __forceinline__ void plan_share(const DecodeArgs &a, int max_len, int64_t &W,
+                                           int &p_eff, int64_t &T0, int64_t &T1, Cursor &c) {
+    __shared__ long long s_wsum[kWarps];
+    __shared__ long long s_scan[kWarps * 32];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int S = a.num_seqs, Hkv = a.num_kv_heads;
+
+    // pass 1: total tiles
+    long long local = 0;
+    for (int s = threadIdx.x; s < S; s += kWarps * 32)
+        local += unit_tiles(clamp_len(a.context_lens, s, max_len));
+#pragma unroll
+    for (int m = 16; m >= 1; m >>= 1) local += __shfl_xor_sync(0xffffffffu, local, m);
+    if (lane == 0) s_wsum[warp] = local;
+    __syncthreads();
+    long long total = 0;
+#pragma unroll
+    for (int i = 0; i < kWarps; ++i) total += s_wsum[i];
+    __syncthreads();
+    W = total * Hkv;
+
+    int64_t pe = W / (a.min_tiles > 0 ? a.min_tiles : 1);
+    if (pe < 1) pe = 1;
+    if (pe > a.num_workers) pe = a.num_workers;
+    p_eff = (int)pe;
+    const int w = blockIdx.x * kWarps + warp;
+    if (w < p_eff) {
+        T0 = (int64_t)w * W / p_eff;
+        T1 = (int64_t)(w + 1) * W / p_eff;
+    } else {
+        T0 = T1 = W;
+    }
+
+    // pass 2: chunked inclusive scan of tiles per sequence; each warp finds
+    // the sequence holding tile T0
+    bool found = T0 >= T1;
+    long long base = 0;
+    for (int c0 = 0; c0 < S; c0 += kWarps * 32) {
+        const int s = c0 + threadIdx.x;
+        long long v = s < S ? unit_tiles(clamp_len(a.context_lens, s, max_len)) : 0;
+#pragma unroll
+        for (int off = 1; off < 32; off <<= 1) {
+            const long long n = __shfl_up_sync(0xffffffffu, v, off);
+            if (lane >= off) v += n;
+        }
+        if (lane == 31) s_wsum[warp] = v;
+        __syncthreads();
+        long long woff = base;
+        for (int i = 0; i < warp; ++i) woff += s_wsum[i];
+        s_scan[threadIdx.x] = v + woff;
+        __syncthreads();
+        const long long chunk_end = s_scan[kWarps * 32 - 1];
+        if (!found && T0 < chunk_end * Hkv) {
+            int hit_i = -1;
+            for (int i0 = 0; i0 < kWarps * 32 && hit_i < 0; i0 += 32) {
+                const unsigned msk = __ballot_sync(0xffffffffu, s_scan[i0 + lane] * Hkv > T0);
+                if (msk) hit_i = i0 + __ffs(msk) - 1;
+            }
+            const long long excl = hit_i == 0 ? base : s_scan[hit_i - 1];
+            const long long nt = s_scan[hit_i] - excl;
+            const long long rem = T0 - excl * Hkv;
+            c.s = c0 + hit_i;
+            c.kvh = (int)(rem / nt);
+            c.j = (int)(rem % nt);
+            c.nt = (int)nt;
+            c.L = clamp_len(a.context_lens, c.s, max_len);
+            found = true;
+        }
+        base = chunk_end;
+        __syncthreads();
+    }
+}
+
+template <class Tile, int GP>
+__global__ void __launch_bounds__(kWarps * 32)
+decode_kernel(const DecodeArgs a) {
+    using Lay = Layout<Tile, GP>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint8_t *ring = smem + warp * Lay::kWarpBytes;
+    float *scratch = reinterpret_cast<float *>(ring + kStages * kStageBytes);
+    float *sm_m = scratch + Tile::kScratchFloats;
+    float *sm_l = sm_m + GP;
+
+    const int max_len = (int)min((int64_t)a.max_blocks_per_seq << a.block_size_log2,
+                                 (int64_t)0x7fffffff);
+    int64_t W, T0, T1;
+    int p_eff;
+    Cursor cc{0, 0, 0, 1, 0};
+    plan_share(a, max_len, W, p_eff, T0, T1, cc);
+    const int w = blockIdx.x * kWarps + warp;
+    if (w >= a.num_workers) return;
+    if (T0 >= T1) {
+        if (lane == 0) a.tasks[w] = make_int4(-1, 0, 0, 0);
+        return;
+    }
+
+    const int g = a.group;
+    const uint16_t *qg = static_cast<const uint16_t *>(a.q);
+    uint32_t *outg = static_cast<uint32_t *>(a.out);
+
+    // producer: runs kStages - 1 tiles ahead of the consumer
+    Cursor pc = cc;
+    int64_t Tp = T0;
+    int p_bid = tile_block(pc, a);
+    int stage_p = 0;
+#pragma unroll
+    for (int i = 0; i < kStages - 1; ++i) {
+        if (Tp < T1) {
+            issue_tile<Tile::kSwizzle>(pc, p_bid, ring + stage_p * kStageBytes, a, lane);
+            cursor_advance(pc, a, max_len);
+            ++Tp;
+            p_bid = Tp < T1 ? tile_block(pc, a) : 0;
+        }
+        cp_async_commit();
+        stage_p = stage_p + 1 == kStages ? 0 : stage_p + 1;
+    }
+
+    Tile tl;
+    int stage_c = 0;
+    int piece = 0;              // index of the current piece within this share
+    bool fresh = true;          // next tile starts a piece
+    int64_t piece_T = T0;       // flat index of the piece's first tile
+    int piece_j0 = 0;
+    int4 task = make_int4(-1, 0, 0, 0);
+
+    for (int64_t T = T0; T < T1; ++T) {
+        if (Tp < T1) {
+            issue_tile<Tile::kSwizzle>(pc, p_bid, ring + stage_p * kStageBytes, a, lane);
+            cursor_advance(pc, a, max_len);
+            ++Tp;
+            p_bid = Tp < T1 ? tile_block(pc, a) : 0;
+        }
+        cp_async_commit();
+        stage_p = stage_p + 1 == kStages ? 0 : stage_p + 1;
+
+        if (fresh) {
+            fresh = false;
+            piece_T = T;
+            piece_j0 = cc.j;
+            tl.begin(qg + ((int64_t)cc.s * a.num_q_heads + (int64_t)cc.kvh * g) * kHeadDim, g, lane);
+        }
+
+        cp_async_wait<kStages - 1>();
+        __syncwarp();
+        uint8_t *stage = ring + stage_c * kStageBytes;
+        tl.tile(stage, tile_valid(cc), a.scale_log2, scratch, lane);
+        stage_c = stage_c + 1 == kStages ? 0 : stage_c + 1;
 
         const bool unit_end = cc.j == cc.nt - 1;
         if (unit_end || T == T1 - 1) {
-            float lt[HP];
-#pragma unroll
-            for (int c = 0; c < HP; ++c) {
-                float x = l_run[c];
-#pragma unroll
-                for (int m = 2; m <= 16; m <<= 1) x += __shfl_xor_sync(0xffffffffu, x, m);
-                lt[c] = x;
-            }
+            // the stage just consumed is refilled only at the next iteration:
+            // it serves as transpose scratch here
+            float oc[GP][4];
+            __syncwarp();
+            tl.finish(reinterpret_cast<float *>(stage), sm_m, sm_l, oc, lane);
+            __syncwarp();
             if (piece_j0 == 0 && unit_end) {
                 // the whole unit is in this share: normalise and write bf16
-                if (t_lane == 0) {
-#pragma unroll
-                    for (int c = 0; c < HP; ++c) sl[hb + c] = lt[c];
-                }
-                __syncwarp();
                 uint32_t *orow = outg + (((int64_t)cc.s * a.num_q_heads + (int64_t)cc.kvh * g) * kHeadDim) / 2;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
                     if (h < g) {
-                        const float l = sl[h];
+                        const float l = sm_l[h];
                         const float inv = l > 0.f ? 1.f / l : 0.f;
                         uint2 pk;
-                        pk.x = pack_bf16x2(o[h][0] * inv, o[h][1] * inv);
-                        pk.y = pack_bf16x2(o[h][2] * inv, o[h][3] * inv);
+                        pk.x = pack_bf16x2(oc[h][0] * inv, oc[h][1] * inv);
+                        pk.y = pack_bf16x2(oc[h][2] * inv, oc[h][3] * inv);
                         reinterpret_cast<uint2 *>(orow + h * (kHeadDim / 2))[lane] = pk;
                     }
                 }
-                __syncwarp();
             } else {
                 // a piece of a unit that other shares continue
                 const int slot = 2 * w + (piece == 0 ? 0 : 1);
@@ -399,13 +599,10 @@ decode_simt_kernel(const DecodeArgs a) {
 #pragma unroll
                 for (int h = 0; h < GP; ++h)
                     reinterpret_cast<float4 *>(po + h * kHeadDim)[lane] =
-                        make_float4(o[h][0], o[h][1], o[h][2], o[h][3]);
-                if (t_lane == 0) {
-#pragma unroll
-                    for (int c = 0; c < HP; ++c)
-                        reinterpret_cast<float2 *>(a.part_ml)[(int64_t)slot * GP + hb + c] =
-                            make_float2(m_run[c], lt[c]);
-                }
+                        make_float4(oc[h][0], oc[h][1], oc[h][2], oc[h][3]);
+                if (lane < GP)
+                    reinterpret_cast<float2 *>(a.part_ml)[(int64_t)slot * GP + lane] =
+                        make_float2(sm_m[lane], sm_l[lane]);
                 if (piece_j0 == 0) {
                     // this share holds the unit's first tile: it owns the combine
                     const int64_t unit_end_T = piece_T + cc.nt;
@@ -413,6 +610,7 @@ decode_simt_kernel(const DecodeArgs a) {
                     task = make_int4(cc.s, cc.kvh, slot, w_last);
                 }
             }
+            __syncwarp();
             ++piece;
             fresh = true;
         }
@@ -437,7 +635,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     uint32_t *orow = static_cast<uint32_t *>(a.out) +
                      (((int64_t)task.x * a.num_q_heads + (int64_t)task.y * g) * kHeadDim) / 2;
     for (int h = 0; h < g; ++h) {
-        float M = -INFINITY;
+        float M = kNegInf;
         for (int i = 0; i < n; ++i) {
             const int slot = i == 0 ? task.z : 2 * (w + i);
             M = fmaxf(M, ml[(int64_t)slot * GP + h].x);
@@ -462,29 +660,26 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     }
 }
 
-template <int GP>
-struct SimtKernel {
-    using Lay = SimtLayout<GP, kSimtWarps, kSimtStages>;
-    static void *fn() { return reinterpret_cast<void *>(&decode_simt_kernel<GP, kSimtWarps, kSimtStages>); }
+template <class Tile, int GP>
+struct Launcher {
+    using Lay = Layout<Tile, GP>;
     static cudaError_t prepare() {
-        return cudaFuncSetAttribute(decode_simt_kernel<GP, kSimtWarps, kSimtStages>,
+        return cudaFuncSetAttribute(decode_kernel<Tile, GP>,
                                     cudaFuncAttributeMaxDynamicSharedMemorySize, Lay::kCtaBytes);
     }
     static int ctas_per_sm() {
         if (prepare() != cudaSuccess) return 0;
         int n = 0;
-        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(
-                &n, decode_simt_kernel<GP, kSimtWarps, kSimtStages>, kSimtWarps * 32,
-                Lay::kCtaBytes) != cudaSuccess)
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, decode_kernel<Tile, GP>, kWarps * 32,
+                                                          Lay::kCtaBytes) != cudaSuccess)
             return 0;
         return n;
     }
     static cudaError_t launch(const DecodeArgs &a, cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        const int grid = (a.num_workers + kSimtWarps - 1) / kSimtWarps;
-        decode_simt_kernel<GP, kSimtWarps, kSimtStages>
-            <<<grid, kSimtWarps * 32, Lay::kCtaBytes, st>>>(a);
+        const int grid = (a.num_workers + kWarps - 1) / kWarps;
+        decode_kernel<Tile, GP><<<grid, kWarps * 32, Lay::kCtaBytes, st>>>(a);
         e = cudaGetLastError();
         if (e != cudaSuccess) return e;
         combine_kernel<GP><<<(a.num_workers + 3) / 4, 128, 0, st>>>(a);
@@ -492,26 +687,49 @@ struct SimtKernel {
     }
 };
 
+template <int GP>
+int ctas_per_sm_for(DecodeKernel k) {
+    return k == DecodeKernel::kSimt ? Launcher<SimtTile<GP>, GP>::ctas_per_sm()
+                                    : Launcher<MmaTile<GP>, GP>::ctas_per_sm();
+}
+
+template <int GP>
+cudaError_t launch_for(const DecodeArgs &a, DecodeKernel k, cudaStream_t st) {
+    return k == DecodeKernel::kSimt ? Launcher<SimtTile<GP>, GP>::launch(a, st)
+                                    : Launcher<MmaTile<GP>, GP>::launch(a, st);
+}
+
+// The CUDA-core tile keeps 16 x GP partial scores per lane: GP = 16 does not fit.
+template <>
+int ctas_per_sm_for<16>(DecodeKernel) {
+    return Launcher<MmaTile<16>, 16>::ctas_per_sm();
+}
+template <>
+cudaError_t launch_for<16>(const DecodeArgs &a, DecodeKernel, cudaStream_t st) {
+    return Launcher<MmaTile<16>, 16>::launch(a, st);
+}
+
 }  // namespace
 
 int decode_group_pad(int group) {
     if (group < 1) return 0;
     int gp = 1;
     while (gp < group) gp <<= 1;
-    return gp <= 8 ? gp : 0;
+    return gp <= 16 ? gp : 0;
 }
 
-int decode_default_workers(int group_pad, int sm_count) {
+int decode_default_workers(int group_pad, DecodeKernel k, int sm_count) {
     int per_sm = 0;
     switch (group_pad) {
-        case 1: per_sm = SimtKernel<1>::ctas_per_sm(); break;
-        case 2: per_sm = SimtKernel<2>::ctas_per_sm(); break;
-        case 4: per_sm = SimtKernel<4>::ctas_per_sm(); break;
-        case 8: per_sm = SimtKernel<8>::ctas_per_sm(); break;
+        case 1: per_sm = ctas_per_sm_for<1>(k); break;
+        case 2: per_sm = ctas_per_sm_for<2>(k); break;
+        case 4: per_sm = ctas_per_sm_for<4>(k); break;
+        case 8: per_sm = ctas_per_sm_for<8>(k); break;
+        case 16: per_sm = ctas_per_sm_for<16>(k); break;
         default: return 0;
     }
     if (per_sm < 1) return 0;
-    return sm_count * per_sm * kSimtWarps;
+    return sm_count * per_sm * kWarps;
 }
 
 size_t decode_workspace_bytes(int group_pad, int num_workers) {
@@ -531,12 +749,13 @@ void decode_carve_workspace(DecodeArgs &a, void *workspace, int group_pad) {
     a.tasks = reinterpret_cast<int4 *>(p);
 }
 
-cudaError_t launch_decode(const DecodeArgs &a, int group_pad, cudaStream_t stream) {
+cudaError_t launch_decode(const DecodeArgs &a, int group_pad, DecodeKernel k, cudaStream_t stream) {
     switch (group_pad) {
-        case 1: return SimtKernel<1>::launch(a, stream);
-        case 2: return SimtKernel<2>::launch(a, stream);
-        case 4: return SimtKernel<4>::launch(a, stream);
-        case 8: return SimtKernel<8>::launch(a, stream);
+        case 1: return launch_for<1>(a, k, stream);
+        case 2: return launch_for<2>(a, k, stream);
+        case 4: return launch_for<4>(a, k, stream);
+        case 8: return launch_for<8>(a, k, stream);
+        case 16: return launch_for<16>(a, k, stream);
         default: return cudaErrorInvalidValue;
     }
 }

@@ -10,6 +10,9 @@ namespace pa {
 constexpr int kHeadDimPublic = 128;   // head_dim the ABI accepts
 constexpr int kDefaultMinTiles = 4;   // automatic shares hold at least this many 16-token tiles
 
+// Tile computation inside the decode worker: tensor cores (mma.sync) or CUDA cores.
+enum class DecodeKernel { kMma = 0, kSimt = 1 };
+
 // Everything one paged-decode launch needs. Pointers are device memory.
 struct DecodeArgs {
     const void *q;              // bf16 [S, Hq, 128]
@@ -33,12 +36,12 @@ struct DecodeArgs {
     int min_tiles;              // fewest tiles a share may hold (1 = exactly P shares)
 };
 
-// Padded group size the kernels are instantiated for (power of two >= group),
-// or 0 when unsupported.
+// Padded group size the kernels are instantiated for (power of two >= group,
+// at most 16), or 0 when unsupported.
 int decode_group_pad(int group);
 
 // Workers (shares) per device when the caller does not force a count.
-int decode_default_workers(int group_pad, int sm_count);
+int decode_default_workers(int group_pad, DecodeKernel k, int sm_count);
 
 // Workspace bytes for P workers at padded group size GP.
 size_t decode_workspace_bytes(int group_pad, int num_workers);
@@ -46,7 +49,7 @@ size_t decode_workspace_bytes(int group_pad, int num_workers);
 // Carve the workspace into DecodeArgs' part_o / part_ml / tasks.
 void decode_carve_workspace(DecodeArgs &a, void *workspace, int group_pad);
 
-cudaError_t launch_decode(const DecodeArgs &a, int group_pad, cudaStream_t stream);
+cudaError_t launch_decode(const DecodeArgs &a, int group_pad, DecodeKernel k, cudaStream_t stream);
 
 cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
                                  const int64_t *slot_mapping, int64_t num_tokens, int row_elems,

@@ -29,7 +29,19 @@ SMALL = {
     "mha": inputs.Spec("mha", ((5, 1, 200),), 8, 8, 16),
     "g8_bs32": inputs.Spec("g8_bs32", ((6, 1, 400),), 64, 8, 32),
     "one_kv_head": inputs.Spec("one_kv_head", ((3, 30, 500),), 4, 1, 64),
+    "g3": inputs.Spec("g3", ((5, 1, 300),), 24, 8, 16),
+    "g5_bs128": inputs.Spec("g5_bs128", ((4, 100, 900),), 40, 8, 128),
+    "g12": inputs.Spec("g12", ((4, 1, 333),), 48, 4, 16),
+    "g16": inputs.Spec("g16", ((6, 1, 700),), 32, 2, 32),
 }
+# tile computations: tensor cores (default) and CUDA cores (group <= 8)
+KERNELS = ["mma", "simt"]
+
+
+@pytest.fixture(params=KERNELS)
+def kernel(request, monkeypatch):
+    monkeypatch.setenv("PA_DECODE_KERNEL", request.param)
+    return request.param
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -38,7 +50,7 @@ def _lib(pa_lib):
 
 
 @pytest.mark.parametrize("name", sorted(SMALL))
-def test_decode_matches_oracle(name):
+def test_decode_matches_oracle(name, kernel):
     wl = inputs.generate(SMALL[name], seed=1)
     ref, kc, vc = pins.run_step(oracle.get(), wl)
     out, gkc, gvc = gu.gpu_step(wl)
@@ -48,7 +60,7 @@ def test_decode_matches_oracle(name):
 
 @pytest.mark.parametrize("name", ["tiny", "large_small", "long_small", "prefix_small"])
 @pytest.mark.parametrize("parts", [1, 2, 7, 64, 5000])
-def test_forced_partitions(name, parts):
+def test_forced_partitions(name, parts, kernel):
     wl = inputs.generate(SMALL[name], seed=2)
     ref, _, _ = pins.run_step(oracle.get(), wl)
     out, _, _ = gu.gpu_step(wl, num_partitions=parts)
@@ -56,7 +68,7 @@ def test_forced_partitions(name, parts):
 
 
 @pytest.mark.parametrize("bs", [16, 64, 256])
-def test_edge_lengths(bs):
+def test_edge_lengths(bs, kernel):
     lens = [0, 1, 2, 15, 16, 17, 31, 32, 33, 255, 256, 257, 0, 1000]
     spec = inputs.Spec("edges", ((len(lens), 1, 1),), 16, 4, bs)
     wl = inputs.generate(spec, seed=3, context_lens=lens)
@@ -77,7 +89,7 @@ def test_store_skips_padding_bit_exact():
     assert np.array_equal(gu.host_bits(d["v_cache"]), vc)
 
 
-def test_single_token_returns_v_row_exactly():
+def test_single_token_returns_v_row_exactly(kernel):
     spec = inputs.Spec("one", ((7, 1, 1),), 32, 8, 16)
     wl = inputs.generate(spec, seed=5)
     out, _, _ = gu.gpu_step(wl)
@@ -86,7 +98,7 @@ def test_single_token_returns_v_row_exactly():
     assert torch.equal(out.view(torch.int16), want.view(torch.int16))
 
 
-def test_unit_values_give_exact_one():
+def test_unit_values_give_exact_one(kernel):
     spec = inputs.scaled(SP["large_batch"], num_seqs=8, ctx_div=4)
     wl = inputs.generate(spec, seed=6, keep_content=True)
     wl = pins._with_values(wl, v_fill=1.0)
@@ -94,7 +106,7 @@ def test_unit_values_give_exact_one():
     assert torch.equal(out, torch.ones_like(out))
 
 
-def test_renumbering_and_private_prefix_are_bit_identical():
+def test_renumbering_and_private_prefix_are_bit_identical(kernel):
     spec = inputs.scaled(SP["prefix_shared"], num_seqs=6, ctx_div=8, store_mode="none",
                          store_rows=0, pad_rows=0)
     wl = inputs.generate(spec, seed=7)
