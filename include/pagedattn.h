@@ -143,6 +143,41 @@ PA_API pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const vo
                              void *workspace, size_t workspace_bytes,
                              int num_partitions, void *stream);
 
+/*
+ * Decode for callers that cannot allocate device memory. The pages have no
+ * counterpart of this call.
+ *
+ * pa_decode needs a caller-provided workspace. Some callers cannot provide
+ * one: they may not call cudaMalloc (or any allocator) on their path, for
+ * example because the call sits in a loop that must not block on the
+ * allocator, or because device memory belongs to a host framework that only
+ * passes in the input and output buffers. This entry point takes the same
+ * inputs and output as pa_decode and allocates nothing: its scratch (the
+ * split-K partial results and combine tasks) is one file-scope array of
+ * PA_NOALLOC_SCRATCH_BYTES bytes in device global memory, which every GPU
+ * that loads the library holds until the process exits.
+ *
+ * - The first call on a device looks up the array's device address (with
+ *   that device current) and caches it; make that first call before any
+ *   stream capture.
+ * - Every call shares the one array. Nothing in it needs to start at zero
+ *   (each call writes every word it later reads), but calls that overlap on
+ *   the GPU (on different streams, or from different threads) race on it
+ *   and give wrong results: serialise them.
+ * - A head configuration whose scratch would exceed the array
+ *   (pa_decode_workspace_size(...) > PA_NOALLOC_SCRATCH_BYTES; on a 152-SM
+ *   GB300 that is a group size above 8) returns PA_ERR_WORKSPACE and
+ *   launches nothing.
+ * Results equal pa_decode's for the same inputs.
+ */
+#define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
+PA_API pa_status_t pa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, int max_blocks_per_seq,
+                                     const int32_t *context_lens, float scale, void *out,
+                                     int num_seqs, int num_q_heads, int num_kv_heads,
+                                     int head_dim, int block_size, int64_t num_blocks,
+                                     void *stream);
+
 #ifdef __cplusplus
 }
 #endif

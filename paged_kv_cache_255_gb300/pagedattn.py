@@ -29,6 +29,8 @@ SIGNATURES = {
                    _P, _SZ, _P], _I32),
     "pa_decode_splitk": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                           _I64, _P, _SZ, _I32, _P], _I32),
+    "pa_decode_noalloc": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32,
+                           _I64, _P], _I32),
 }
 
 _lock = threading.Lock()
