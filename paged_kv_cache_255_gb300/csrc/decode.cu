@@ -165,7 +165,7 @@ struct MmaTile {
                                          float *, int lane) {
         const uint32_t base = smem_u32(stage);
         const int i7 = lane & 7, mi = lane >> 3;
-        const int gid = lane >> 2, tig = lane & 3;
+        const int gid = lane >> 2;
 
         float s[NT][4];
 #pragma unroll
@@ -505,6 +505,13 @@ decode_kernel(const DecodeArgs a) {
     float *sm_m = scratch + Tile::kScratchFloats;
     float *sm_l = sm_m + GP;
 
+    // Launched as a programmatic dependent of the previous kernel in the
+    // stream (normally the store of this step's K/V rows): wait until that
+    // kernel has finished and its writes are visible before reading anything,
+    // then let the combine launch queue up behind this grid.
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+
     const int max_len = (int)min((int64_t)a.max_blocks_per_seq << a.block_size_log2,
                                  (int64_t)0x7fffffff);
     int64_t W, T0, T1;
@@ -624,6 +631,9 @@ decode_kernel(const DecodeArgs a) {
 // task; lane l handles dims [4l, 4l + 4) of each query head.
 template <int GP>
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
+    // programmatic dependent of the decode grid: wait for all of it (and its
+    // writes) before reading any task or partial result
+    asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int w = blockIdx.x * 4 + warp;
     if (w >= a.num_workers) return;
@@ -675,14 +685,34 @@ struct Launcher {
             return 0;
         return n;
     }
+    // Both kernels go out as programmatic dependent launches: each may be
+    // scheduled while the kernel before it in the stream is still running, and
+    // waits for it (griddepcontrol.wait) before touching its results.
+    static cudaError_t launch_pdl(const void *fn, unsigned grid, unsigned block, size_t smem,
+                                  const DecodeArgs &a, cudaStream_t st) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(block);
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = st;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+        attr[0].val.programmaticStreamSerializationAllowed = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        void *args[] = {const_cast<DecodeArgs *>(&a)};
+        return cudaLaunchKernelExC(&cfg, fn, args);
+    }
     static cudaError_t launch(const DecodeArgs &a, cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
-        const int grid = (a.num_workers + kWarps - 1) / kWarps;
-        decode_kernel<Tile, GP><<<grid, kWarps * 32, Lay::kCtaBytes, st>>>(a);
-        e = cudaGetLastError();
+        const unsigned grid = (a.num_workers + kWarps - 1) / kWarps;
+        e = launch_pdl(reinterpret_cast<const void *>(&decode_kernel<Tile, GP>), grid,
+                       kWarps * 32, Lay::kCtaBytes, a, st);
         if (e != cudaSuccess) return e;
-        combine_kernel<GP><<<(a.num_workers + 3) / 4, 128, 0, st>>>(a);
+        e = launch_pdl(reinterpret_cast<const void *>(&combine_kernel<GP>),
+                       (a.num_workers + 3) / 4, 128, 0, a, st);
+        if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
 };

@@ -20,6 +20,9 @@ store_kvcache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                      uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                      const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
                      int row_chunks, int64_t num_slots) {
+    // let a decode launched as a programmatic dependent start its launch now;
+    // it still waits for this grid to finish before reading the cache
+    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int lane = threadIdx.x & 31;
     const int64_t first = (int64_t)blockIdx.x * kStoreWarps + (threadIdx.x >> 5);
     const int64_t stride = (int64_t)gridDim.x * kStoreWarps;
