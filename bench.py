@@ -184,10 +184,13 @@ def oracle_sample(wl, target_s: float, host=None):
     work_all = float(wl.context_lens.astype(np.float64).sum()) * Hq
     rng = np.random.Generator(np.random.PCG64(123))
     order = rng.permutation(S * Hq)
-    done_pairs, done_work, elapsed = 0, 0.0, 0.0
+    done_pairs, done_work, elapsed, passes = 0, 0.0, 0.0, 0
     batch = max(threads, 8)
-    while elapsed < target_s and done_pairs < S * Hq:
-        idx = order[done_pairs:done_pairs + batch]
+    # random (sequence, head) outputs, in growing batches, until target_s of
+    # oracle time; a workload smaller than that is repeated whole
+    while elapsed < target_s:
+        pos = done_pairs % (S * Hq)
+        idx = order[pos:pos + batch]
         pairs = np.stack([idx // Hq, idx % Hq], 1).astype(np.int32)
         t0 = time.perf_counter()
         O.decode_pairs(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale, pairs, threads=0)
@@ -198,8 +201,8 @@ def oracle_sample(wl, target_s: float, host=None):
     decode_s = elapsed * (work_all / max(done_work, 1.0))
     us = (t_store + decode_s) * 1e6
     sample = (f"oracle store of all {int(wl.slot_mapping.shape[0])} rows + decode of "
-              f"{done_pairs}/{S * Hq} random (seq, q-head) outputs ({elapsed:.1f} s), scaled by "
-              f"context tokens to the full step")
+              f"{done_pairs} random (seq, q-head) outputs out of {S * Hq} per step "
+              f"({elapsed:.1f} s of oracle time), scaled by context tokens to one full step")
     return us, threads, sample
 
 
@@ -216,9 +219,10 @@ def run_reference(args, rank, world):
     wl = inputs.generate(workload_spec(args), seed=0,
                          device="cuda" if torch.cuda.is_available() else "cpu")
     host = (wl.q.cpu(), wl.k_cache.cpu(), wl.v_cache.cpu(), wl.k_new.cpu(), wl.v_new.cpu())
-    per_step = max(1.0, args.ref_seconds / max(1, args.steps))
+    # the whole run (warm-up and timed steps) takes about --ref-seconds of oracle time
+    per_step = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
-        oracle_sample(wl, 0.2, host)
+        oracle_sample(wl, per_step, host)
     vals = []
     for _ in range(args.steps):
         us, threads, sample = oracle_sample(wl, per_step, host)
