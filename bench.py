@@ -261,14 +261,30 @@ def run_gpu(args, rank, world, local):
             pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots)
         pa.decode(q, k_cache, v_cache, bt, cl, wl.scale, out=out, workspace=ws)
 
-    # ---- device-resident timing
+    # ---- device-resident timing: store then decode back to back, as a user
+    # issues them (the decode launch may overlap the store's tail)
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
     clocks = ClockSampler(local)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world)
+
+    # ---- the same steps with an event between store and decode, for the
+    # per-call split and the decode launch's own bandwidth (roofline)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     torch.cuda.synchronize()
     for i in range(args.steps):
         flush.zero_()
@@ -279,29 +295,32 @@ def run_gpu(args, rank, world, local):
         pa.decode(q, k_cache, v_cache, bt, cl, wl.scale, out=out, workspace=ws)
         ev[i][2].record(stream)
     torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
     store_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
     dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    step_ms = [ev[i][0].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    ms = max_over_ranks(sum(step_ms) / len(step_ms), world)
     dec_avg = max_over_ranks(sum(dec_ms) / len(dec_ms), world)
     store_avg = max_over_ranks(sum(store_ms) / len(store_ms), world)
 
-    # ---- end to end through host buffers
-    hq = q.cpu().pin_memory()
-    hk, hv = k_new.cpu().pin_memory(), v_new.cpu().pin_memory()
-    hs = slots.cpu().pin_memory()
-    hbt, hcl = bt.cpu().pin_memory(), cl.cpu().pin_memory()
+    # ---- end to end through host buffers: the step's inputs are packed in one
+    # pinned staging buffer, copied in one transfer, and the output read back
+    host_inputs = [q, k_new, v_new, slots, bt, cl]
+    offs, total = [], 0
+    for t in host_inputs:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_stage = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    for t, o in zip(host_inputs, offs):
+        n = t.numel() * t.element_size()
+        h_stage[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+    d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = [d_stage[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+             for t, o in zip(host_inputs, offs)]
+    dq, dk, dv, ds, dbt, dcl = views
     hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    dq, dk, dv = torch.empty_like(q), torch.empty_like(k_new), torch.empty_like(v_new)
-    ds, dbt, dcl = torch.empty_like(slots), torch.empty_like(bt), torch.empty_like(cl)
-    h2d = sum(t.numel() * t.element_size() for t in (hq, hk, hv, hs, hbt, hcl))
+    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
-        for d_, h_ in ((dq, hq), (dk, hk), (dv, hv), (ds, hs), (dbt, hbt), (dcl, hcl)):
-            d_.copy_(h_, non_blocking=True)
+        d_stage.copy_(h_stage, non_blocking=True)
         if has_store:
             pa.store_kvcache(dk, dv, k_cache, v_cache, ds)
         pa.decode(dq, k_cache, v_cache, dbt, dcl, wl.scale, out=out, workspace=ws)
@@ -321,6 +340,9 @@ def run_gpu(args, rank, world, local):
         b_.synchronize()
         e2e_ms.append(a_.elapsed_time(b_))
     e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
+    torch.cuda.synchronize()
+    if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
+        raise SystemExit("e2e output differs from the device-resident output")
 
     if rank != 0:
         return
@@ -342,6 +364,8 @@ def run_gpu(args, rank, world, local):
         "e2e": {"value": e2e * 1e3, "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * (3 if has_store else 2),
+        "timing": "value: store + decode back to back per step; store_us / decode_us: a "
+                  "second pass with an event between the two calls",
         "clocks": clk,
     }
     if not args.no_cpu_baseline and world >= 1:

@@ -494,6 +494,23 @@ __device__ __forceinline__ void plan_share(const DecodeArgs &a, int max_len, int
     }
 }
 
+// L2 prefetch of context_lens, block_tables and q, in 128-byte lines spread
+// over every thread of the grid.
+__device__ __forceinline__ void prefetch_inputs(const DecodeArgs &a) {
+    const int64_t n_cl = ((int64_t)a.num_seqs * 4 + 127) >> 7;
+    const int64_t n_bt = ((int64_t)a.num_seqs * a.max_blocks_per_seq * 4 + 127) >> 7;
+    const int64_t n_q = ((int64_t)a.num_seqs * a.num_q_heads * kRowBytes + 127) >> 7;
+    const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+    for (int64_t i = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n_cl + n_bt + n_q;
+         i += stride) {
+        const char *p = i < n_cl ? reinterpret_cast<const char *>(a.context_lens) + (i << 7)
+                      : i < n_cl + n_bt
+                          ? reinterpret_cast<const char *>(a.block_tables) + ((i - n_cl) << 7)
+                          : static_cast<const char *>(a.q) + ((i - n_cl - n_bt) << 7);
+        asm volatile("prefetch.global.L2 [%0];\n" ::"l"(p));
+    }
+}
+
 template <class Tile, int GP>
 __global__ void __launch_bounds__(kWarps * 32)
 decode_kernel(const DecodeArgs a) {
@@ -506,9 +523,13 @@ decode_kernel(const DecodeArgs a) {
     float *sm_l = sm_m + GP;
 
     // Launched as a programmatic dependent of the previous kernel in the
-    // stream (normally the store of this step's K/V rows): wait until that
-    // kernel has finished and its writes are visible before reading anything,
-    // then let the combine launch queue up behind this grid.
+    // stream (normally the store of this step's K/V rows). While that kernel
+    // may still run, pull this launch's small inputs (lengths, tables, q) into
+    // L2; a prefetch reads nothing into registers, and L2 is the point of
+    // coherence, so a later write by that kernel still wins. Then wait until
+    // it has finished and its writes are visible before reading anything, and
+    // let the combine launch queue up behind this grid.
+    prefetch_inputs(a);
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
 
