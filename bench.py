@@ -344,6 +344,34 @@ def run_gpu(args, rank, world, local):
     if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
         raise SystemExit("e2e output differs from the device-resident output")
 
+    # ---- the same two steps replayed from CUDA graphs (one launch per step)
+    def time_replay(g):
+        for _ in range(args.warmup):
+            flush.zero_()
+            g.replay()
+        torch.cuda.synchronize()
+        t = []
+        for _ in range(args.steps):
+            flush.zero_()
+            a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a_.record(stream)
+            g.replay()
+            b_.record(stream)
+            b_.synchronize()
+            t.append(a_.elapsed_time(b_))
+        return max_over_ranks(sum(t) / len(t), world)
+
+    g_dev = pa.DecodeStepGraph(q, k_cache, v_cache, bt, cl, wl.scale, k_new=k_new, v_new=v_new,
+                               slot_mapping=slots if has_store else None, out=out)
+    graph_ms = time_replay(g_dev)
+    g_e2e = pa.DecodeStepGraph(dq, k_cache, v_cache, dbt, dcl, wl.scale, k_new=dk, v_new=dv,
+                               slot_mapping=ds if has_store else None, out=out,
+                               host_stage=h_stage, device_stage=d_stage, host_out=hout)
+    graph_e2e_ms = time_replay(g_e2e)
+    torch.cuda.synchronize()
+    if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
+        raise SystemExit("graph e2e output differs from the device-resident output")
+
     if rank != 0:
         return
     kv_bytes = wl.kv_bytes()
@@ -363,6 +391,9 @@ def run_gpu(args, rank, world, local):
                      "algorithmic_bytes": kv_bytes, "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": e2e * 1e3, "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
+        "graph": {"us_per_step": graph_ms * 1e3, "e2e_us_per_step": graph_e2e_ms * 1e3,
+                  "note": "store + decode (and, for e2e, the H2D and D2H copies) captured "
+                          "in one CUDA graph, one replay per step"},
         "gpu_launches": args.steps * (3 if has_store else 2),
         "timing": "value: store + decode back to back per step; store_us / decode_us: a "
                   "second pass with an event between the two calls",

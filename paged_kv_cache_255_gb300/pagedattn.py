@@ -176,3 +176,54 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
             st = lib().pa_decode(*args, _stream_ptr(stream, dev))
     _check("pa_decode", st)
     return out
+
+
+class DecodeStepGraph:
+    """One decode step (store of the new K/V rows, then decode) captured into a
+    CUDA graph and replayed with one launch per step.
+
+    The tensors passed in are the graph's fixed buffers: update their contents
+    in place (q, k_new, v_new, slot_mapping, block_tables, context_lens) and
+    call replay(); the result lands in ``out``. With ``host_stage`` (a pinned
+    uint8 tensor) and ``device_stage`` (a device uint8 tensor of the same size
+    whose slices back the input tensors), the host-to-device copy of the step's
+    inputs is captured too, and with ``host_out`` (pinned) the read-back of
+    ``out``: one replay is then the whole step from host buffers to host
+    buffers. The decode is the automatic-partition pa_decode; its workspace is
+    allocated once here, before capture.
+    """
+
+    def __init__(self, q, k_cache, v_cache, block_tables, context_lens, scale, k_new=None,
+                 v_new=None, slot_mapping=None, out=None, host_stage=None, device_stage=None,
+                 host_out=None):
+        dev = q.device
+        S, Hq, D = q.shape
+        Hkv = k_cache.shape[2]
+        self.out = out if out is not None else torch.empty_like(q)
+        self.workspace = workspace_for(Hq, Hkv, D, 0, dev)
+        has_store = slot_mapping is not None and slot_mapping.shape[0] > 0
+
+        def body():
+            if host_stage is not None:
+                device_stage.copy_(host_stage, non_blocking=True)
+            if has_store:
+                store_kvcache(k_new, v_new, k_cache, v_cache, slot_mapping)
+            decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=self.out,
+                   workspace=self.workspace)
+            if host_out is not None:
+                host_out.copy_(self.out, non_blocking=True)
+
+        # one eager run first: library set-up calls happen outside the capture
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            body()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        self.graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.graph):
+            body()
+
+    def replay(self):
+        self.graph.replay()
+        return self.out
