@@ -82,6 +82,9 @@ class Oracle:
         lib.oracle_decode_pairs.argtypes = [p, p, p, p, i32, p, dbl, p, i64, p, i32, i32, i32,
                                             i32, i32, i64, i32]
         lib.oracle_decode_pairs.restype = i32
+        lib.oracle_decode_multi.argtypes = [p, p, p, p, i32, p, i32, dbl, p, i32, i32, i32, i32,
+                                            i32, i64, i32]
+        lib.oracle_decode_multi.restype = i32
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         self.lib = lib
@@ -156,6 +159,24 @@ class Oracle:
         return out
 
 
+    def decode_multi(self, q, k_cache, v_cache, block_tables, context_lens, scale,
+                     threads: int = 0):
+        """fp64 [S, Q, Hq, D] outputs for Q new tokens per sequence (q is
+        [S, Q, Hq, D]); token i attends to keys t <= L - Q + i."""
+        qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+        bt = _arr(block_tables, np.int32)
+        cl = _arr(context_lens, np.int32)
+        S, Q, Hq, D = qb.shape
+        NB, bs, Hkv, _ = kc.shape
+        out = np.zeros((S, Q, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_decode_multi(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                                          _ptr(cl), Q, float(scale), _ptr(out), S, Hq, Hkv, D,
+                                          bs, NB, int(threads))
+        if rc != OK:
+            raise OracleError(f"oracle_decode_multi returned {rc}")
+        return out
+
+
 def compile_variant(src: str, out_path: str) -> "Oracle":
     """Compile another copy of the oracle source (the tests plant mistakes in
     copies to check that the pins catch them) and bind it."""
@@ -188,3 +209,7 @@ def decode(*a, **kw):
 
 def decode_pairs(*a, **kw):
     return get().decode_pairs(*a, **kw)
+
+
+def decode_multi(*a, **kw):
+    return get().decode_multi(*a, **kw)

@@ -79,17 +79,20 @@ int oracle_store_kvcache(const uint16_t *k, const uint16_t *v,
     return ORACLE_OK;
 }
 
-/* One output row: query head h of sequence s, written to out[0..head_dim). */
+/* One output row: query head h of query row q_index, attending to the first
+ * min(context_lens[s], cap) tokens of sequence s, written to out[0..head_dim).
+ * Single-token decode has q_index = s and cap = context_lens[s]. */
 static int decode_one(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
                       const int32_t *block_tables, int max_blocks_per_seq,
                       const int32_t *context_lens, double scale,
                       int s, int h, int num_q_heads, int num_kv_heads, int head_dim,
-                      int block_size, int64_t num_blocks, double *out)
+                      int block_size, int64_t num_blocks, int q_index, int cap, double *out)
 {
     const int group = num_q_heads / num_kv_heads;
     const int kvh = h / group;
-    const int L = context_lens[s];
-    const uint16_t *qrow = q + ((int64_t)s * num_q_heads + h) * head_dim;
+    const int L = context_lens[s] < 0 || context_lens[s] <= cap ? context_lens[s]
+                                                                 : (cap > 0 ? cap : 0);
+    const uint16_t *qrow = q + ((int64_t)q_index * num_q_heads + h) * head_dim;
 
     for (int d = 0; d < head_dim; ++d)
         out[d] = 0.0;
@@ -168,9 +171,11 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
 #pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
 #endif
     for (int64_t i = 0; i < total; ++i) {
+        const int s = (int)(i / num_q_heads);
         int r = decode_one(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                           scale, (int)(i / num_q_heads), (int)(i % num_q_heads), num_q_heads,
-                           num_kv_heads, head_dim, block_size, num_blocks, out + i * head_dim);
+                           scale, s, (int)(i % num_q_heads), num_q_heads, num_kv_heads,
+                           head_dim, block_size, num_blocks, s, context_lens[s],
+                           out + i * head_dim);
         if (r != ORACLE_OK) {
 #ifdef _OPENMP
 #pragma omp critical
@@ -206,7 +211,55 @@ int oracle_decode_pairs(const uint16_t *q, const uint16_t *k_cache, const uint16
     for (int64_t i = 0; i < num_pairs; ++i) {
         int r = decode_one(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            scale, pairs[2 * i], pairs[2 * i + 1], num_q_heads, num_kv_heads,
-                           head_dim, block_size, num_blocks, out + i * head_dim);
+                           head_dim, block_size, num_blocks, pairs[2 * i],
+                           context_lens[pairs[2 * i]], out + i * head_dim);
+        if (r != ORACLE_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            err = r;
+        }
+    }
+    (void)num_threads;
+    return err;
+}
+
+/*
+ * Several new tokens per sequence (the verification step of speculative
+ * decoding, "Implementation Details", Speculative Decoding -- EAGLE Proposer:
+ * draft tokens are checked by the target model in one pass). Query token i of
+ * the q_len new tokens of sequence s sits at position L - q_len + i, where L =
+ * context_lens[s] counts them all, and attends causally to tokens
+ * t <= L - q_len + i; a query with no such token outputs zero.
+ * q and out are [num_seqs, q_len, num_q_heads, head_dim].
+ */
+int oracle_decode_multi(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *context_lens, int q_len, double scale, double *out,
+                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int block_size, int64_t num_blocks, int num_threads)
+{
+    int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_blocks_per_seq);
+    if (rc != ORACLE_OK)
+        return rc;
+    if (q_len < 1)
+        return ORACLE_ERR_ARG;
+    const int64_t total = (int64_t)num_seqs * q_len * num_q_heads;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    if (num_threads <= 0)
+        num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 1) num_threads(num_threads)
+#endif
+    for (int64_t r_i = 0; r_i < total; ++r_i) {
+        const int64_t row = r_i / num_q_heads;          /* s * q_len + i */
+        const int s = (int)(row / q_len), i = (int)(row % q_len);
+        const int cap = context_lens[s] - q_len + i + 1;
+        int r = decode_one(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                           scale, s, (int)(r_i % num_q_heads), num_q_heads, num_kv_heads,
+                           head_dim, block_size, num_blocks, (int)row, cap,
+                           out + r_i * head_dim);
         if (r != ORACLE_OK) {
 #ifdef _OPENMP
 #pragma omp critical

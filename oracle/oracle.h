@@ -50,6 +50,15 @@ int oracle_decode_pairs(const uint16_t *q, const uint16_t *k_cache, const uint16
                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                         int block_size, int64_t num_blocks, int num_threads);
 
+/* Several new tokens per sequence: query token i of the q_len new tokens of
+ * sequence s attends causally to tokens t <= context_lens[s] - q_len + i.
+ * q and out are [num_seqs, q_len, num_q_heads, head_dim]. */
+int oracle_decode_multi(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                        const int32_t *block_tables, int max_blocks_per_seq,
+                        const int32_t *context_lens, int q_len, double scale, double *out,
+                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int block_size, int64_t num_blocks, int num_threads);
+
 /* Threads the OpenMP loops use by default. */
 int oracle_num_threads(void);
 

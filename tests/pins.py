@@ -272,6 +272,60 @@ def pin_store(O):
             assert np.array_equal(got.reshape(NB * bs, Hkv * D), want), f"{spec.name}: store"
 
 
+def _multi_workload(spec, seed, Q):
+    """A decode step with Q new query tokens per sequence (q: [S, Q, Hq, D])."""
+    wl = inputs.generate(spec, seed=seed, keep_content=True)
+    g = torch.Generator().manual_seed(seed)
+    S, Hq, D = wl.q.shape
+    q = torch.randn((S, Q, Hq, D), generator=g).to(BF16)
+    return wl, q
+
+
+def pin_multi_sdpa(O):
+    """Q new tokens per sequence against torch's fp64 SDPA with an explicit
+    causal mask: token i sees keys t <= L - Q + i."""
+    for spec, Q in ((inputs.SPECS["tiny"], 3),
+                    (inputs.scaled(inputs.SPECS["large_batch"], num_seqs=5, ctx_div=16), 4),
+                    (inputs.Spec("mq", ((4, 1, 40),), 8, 2, 16), 2)):
+        wl, q = _multi_workload(spec, 31, Q)
+        kc, vc = wl.k_cache, wl.v_cache
+        if wl.slot_mapping.shape[0]:
+            kc, vc = O.store_kvcache(wl.k_new, wl.v_new, kc, vc, wl.slot_mapping)
+        out = O.decode_multi(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+        for i in range(wl.num_seqs):
+            L = int(wl.context_lens[i])
+            if L == 0:
+                assert np.all(out[i] == 0)
+                continue
+            k, v = wl.logical_kv(i)
+            qq = q[i].double().permute(1, 0, 2)[None]          # [1, Hq, Q, D]
+            kk = k.double().permute(1, 0, 2)[None]
+            vv = v.double().permute(1, 0, 2)[None]
+            pos = torch.arange(L)[None, :]
+            lim = (L - Q + torch.arange(Q))[:, None]
+            mask = pos <= lim                                  # [Q, L]
+            ref = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=wl.scale,
+                                                 enable_gqa=True)[0].permute(1, 0, 2).numpy()
+            seen = (lim[:, 0] >= 0).numpy()
+            err = np.abs(out[i][seen] - np.nan_to_num(ref[seen])).max() if seen.any() else 0.0
+            assert err <= 1e-10, f"{spec.name}: multi-token vs SDPA max err {err}"
+            assert np.all(out[i][~seen] == 0)
+
+
+def pin_multi_prefix(O):
+    """Query token i of Q equals a single-token decode of the same query row
+    over the sequence cut to its first L - Q + i + 1 tokens."""
+    spec = inputs.scaled(inputs.SPECS["qwen3_0_6b"], num_seqs=4, ctx_div=8)
+    Q = 3
+    wl, q = _multi_workload(spec, 32, Q)
+    kc, vc = O.store_kvcache(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping)
+    out = O.decode_multi(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+    for i in range(Q):
+        cut = np.maximum(wl.context_lens - Q + i + 1, 0).astype(np.int32)
+        single = O.decode(q[:, i].contiguous(), kc, vc, wl.block_tables, cut, wl.scale)
+        assert np.array_equal(out[:, i], single), f"query token {i}"
+
+
 ALL_PINS = [pin_sdpa, pin_single_token, pin_zero_keys, pin_unit_values, pin_three_tokens,
             pin_dominant_key, pin_renumbering, pin_prefix_private, pin_block_size,
-            pin_nan_free, pin_store]
+            pin_nan_free, pin_store, pin_multi_sdpa, pin_multi_prefix]

@@ -20,8 +20,12 @@ MUTANTS = [
     ("scale_dropped", "score[t] = scale * dot;", "score[t] = dot;"),
     ("not_normalised", "double p = score[t] / denom;", "double p = score[t];"),
     ("last_token_dropped", "t < L;", "t < L - 1;"),
-    ("query_row_of_kv_head", "(int64_t)s * num_q_heads + h) * head_dim",
-     "(int64_t)s * num_q_heads + kvh) * head_dim"),
+    ("query_row_of_kv_head", "(int64_t)q_index * num_q_heads + h) * head_dim",
+     "(int64_t)q_index * num_q_heads + kvh) * head_dim"),
+    ("causal_diagonal_dropped", "const int cap = context_lens[s] - q_len + i + 1;",
+     "const int cap = context_lens[s] - q_len + i;"),
+    ("causal_mask_ignored", "const int cap = context_lens[s] - q_len + i + 1;",
+     "const int cap = context_lens[s];"),
     ("store_v_from_k", "memcpy(v_cache + slot * row, v + i * row",
      "memcpy(v_cache + slot * row, k + i * row"),
     ("store_skips_first_row", "if (slot == -1)\n            continue;",
