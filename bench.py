@@ -250,8 +250,19 @@ def run_gpu(args, rank, world, local):
     slots = torch.from_numpy(wl.slot_mapping).to(dev)
     bt = torch.from_numpy(wl.block_tables).to(dev)
     cl = torch.from_numpy(wl.context_lens).to(dev)
+    Q = args.q_len
+    if Q > 1:
+        # Q query tokens per sequence (speculative verification)
+        gq = torch.Generator(device=dev)
+        gq.manual_seed(1)
+        q = torch.randn((S, Q, Hq, D), generator=gq, device=dev).to(torch.bfloat16)
     out = torch.empty_like(q)
     ws = pa.workspace_for(Hq, Hkv, D, 0, dev)
+
+    def decode_call(q_, bt_, cl_):
+        if Q > 1:
+            return pa.decode_multi(q_, k_cache, v_cache, bt_, cl_, wl.scale, out=out)
+        return pa.decode(q_, k_cache, v_cache, bt_, cl_, wl.scale, out=out, workspace=ws)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     has_store = slots.shape[0] > 0
@@ -259,7 +270,7 @@ def run_gpu(args, rank, world, local):
     def step():
         if has_store:
             pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots)
-        pa.decode(q, k_cache, v_cache, bt, cl, wl.scale, out=out, workspace=ws)
+        decode_call(q, bt, cl)
 
     # ---- device-resident timing: store then decode back to back, as a user
     # issues them (the decode launch may overlap the store's tail)
@@ -292,7 +303,7 @@ def run_gpu(args, rank, world, local):
         if has_store:
             pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots)
         ev[i][1].record(stream)
-        pa.decode(q, k_cache, v_cache, bt, cl, wl.scale, out=out, workspace=ws)
+        decode_call(q, bt, cl)
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     store_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
@@ -323,7 +334,7 @@ def run_gpu(args, rank, world, local):
         d_stage.copy_(h_stage, non_blocking=True)
         if has_store:
             pa.store_kvcache(dk, dv, k_cache, v_cache, ds)
-        pa.decode(dq, k_cache, v_cache, dbt, dcl, wl.scale, out=out, workspace=ws)
+        decode_call(dq, dbt, dcl)
         hout.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -361,16 +372,22 @@ def run_gpu(args, rank, world, local):
             t.append(a_.elapsed_time(b_))
         return max_over_ranks(sum(t) / len(t), world)
 
-    g_dev = pa.DecodeStepGraph(q, k_cache, v_cache, bt, cl, wl.scale, k_new=k_new, v_new=v_new,
-                               slot_mapping=slots if has_store else None, out=out)
-    graph_ms = time_replay(g_dev)
-    g_e2e = pa.DecodeStepGraph(dq, k_cache, v_cache, dbt, dcl, wl.scale, k_new=dk, v_new=dv,
-                               slot_mapping=ds if has_store else None, out=out,
-                               host_stage=h_stage, device_stage=d_stage, host_out=hout)
-    graph_e2e_ms = time_replay(g_e2e)
-    torch.cuda.synchronize()
-    if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
-        raise SystemExit("graph e2e output differs from the device-resident output")
+    def time_graphs():
+        g_dev = pa.DecodeStepGraph(q, k_cache, v_cache, bt, cl, wl.scale, k_new=k_new, v_new=v_new,
+                                   slot_mapping=slots if has_store else None, out=out)
+        graph_ms = time_replay(g_dev)
+        g_e2e = pa.DecodeStepGraph(dq, k_cache, v_cache, dbt, dcl, wl.scale, k_new=dk, v_new=dv,
+                                   slot_mapping=ds if has_store else None, out=out,
+                                   host_stage=h_stage, device_stage=d_stage, host_out=hout)
+        graph_e2e_ms = time_replay(g_e2e)
+        torch.cuda.synchronize()
+        if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
+            raise SystemExit("graph e2e output differs from the device-resident output")
+        return graph_ms, graph_e2e_ms
+
+    graph_ms = graph_e2e_ms = float("nan")
+    if Q == 1:
+        graph_ms, graph_e2e_ms = time_graphs()
 
     if rank != 0:
         return
@@ -381,7 +398,7 @@ def run_gpu(args, rank, world, local):
         "metric": METRIC, "value": ms * 1e3, "unit": "us/step", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": workload_config(wl),
+        "data": "synthetic", "config": dict(workload_config(wl), q_len=Q),
         "store_us": store_avg * 1e3, "decode_us": dec_avg * 1e3,
         "kv_read_gbs": achieved, "hbm_frac": achieved / peak,
         "unique_kv_read_gbs": wl.unique_kv_bytes() / (dec_avg * 1e-3) / 1e9,
@@ -391,7 +408,8 @@ def run_gpu(args, rank, world, local):
                      "algorithmic_bytes": kv_bytes, "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": e2e * 1e3, "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "graph": {"us_per_step": graph_ms * 1e3, "e2e_us_per_step": graph_e2e_ms * 1e3,
+        "graph": {"us_per_step": graph_ms * 1e3 if Q == 1 else None,
+                  "e2e_us_per_step": graph_e2e_ms * 1e3 if Q == 1 else None,
                   "note": "store + decode (and, for e2e, the H2D and D2H copies) captured "
                           "in one CUDA graph, one replay per step"},
         "gpu_launches": args.steps * (3 if has_store else 2),
@@ -414,6 +432,8 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.SPECS))
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="run a copy of the workload with this many sequences (profiling)")
+    ap.add_argument("--q-len", type=int, default=1,
+                    help="query tokens per sequence (speculative verification); 1 = decode")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)

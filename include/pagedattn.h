@@ -178,6 +178,32 @@ PA_API pa_status_t pa_decode_noalloc(const void *q, const void *k_cache, const v
                                      int head_dim, int block_size, int64_t num_blocks,
                                      void *stream);
 
+/*
+ * Decode of several new tokens per sequence at once: the verification pass of
+ * speculative decoding, where the target model checks q_len draft tokens of
+ * each sequence in one step ("Implementation Details", Speculative Decoding --
+ * EAGLE Proposer: draft tokens proposed, then verified by the target model).
+ *
+ * q and out are [num_seqs, q_len, num_q_heads, head_dim] bf16. context_lens[s]
+ * counts all q_len new tokens (they are stored in the cache before the call,
+ * e.g. with pa_store_kvcache); query token i sits at position
+ * context_lens[s] - q_len + i and attends causally to tokens
+ * t <= context_lens[s] - q_len + i, gathered as in pa_decode. A query token
+ * with no such token outputs zero. q_len = 1 is pa_decode.
+ *
+ * Requirements: as pa_decode, plus 1 <= q_len and q_len * (num_q_heads /
+ * num_kv_heads) <= 16; the workspace must hold
+ * pa_decode_multi_workspace_size(q_len, ...) bytes. Always the tensor-core path.
+ */
+PA_API size_t pa_decode_multi_workspace_size(int q_len, int num_q_heads, int num_kv_heads,
+                                             int head_dim);
+PA_API pa_status_t pa_decode_multi(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, int q_len, float scale,
+                                   void *out, int num_seqs, int num_q_heads, int num_kv_heads,
+                                   int head_dim, int block_size, int64_t num_blocks,
+                                   void *workspace, size_t workspace_bytes, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

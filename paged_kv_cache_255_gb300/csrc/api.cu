@@ -30,9 +30,10 @@ int current_sm_count() {
 // Tile computation for decode: tensor cores unless PA_DECODE_KERNEL=simt asks
 // for the CUDA-core variant (kept for comparison and testing). Group sizes
 // above 8 always use the tensor cores.
-pa::DecodeKernel decode_kernel_choice(int group_pad) {
+pa::DecodeKernel decode_kernel_choice(int group_pad, int q_len) {
     const char *e = std::getenv("PA_DECODE_KERNEL");
-    if (e && std::strcmp(e, "simt") == 0 && group_pad <= 8) return pa::DecodeKernel::kSimt;
+    if (e && std::strcmp(e, "simt") == 0 && group_pad <= 8 && q_len == 1)
+        return pa::DecodeKernel::kSimt;
     return pa::DecodeKernel::kMma;
 }
 
@@ -45,17 +46,18 @@ int plan_workers(int group_pad, pa::DecodeKernel k, int num_partitions) {
 
 pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
                         const int32_t *block_tables, int max_blocks_per_seq,
-                        const int32_t *context_lens, float scale, void *out, int num_seqs,
-                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                        int64_t num_blocks, void *workspace, size_t workspace_bytes,
-                        int num_partitions, void *stream) {
+                        const int32_t *context_lens, int q_len, float scale, void *out,
+                        int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                        int block_size, int64_t num_blocks, void *workspace,
+                        size_t workspace_bytes, int num_partitions, void *stream) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 ||
-        max_blocks_per_seq < 0 || num_partitions < 0 || !std::isfinite(scale))
+        max_blocks_per_seq < 0 || num_partitions < 0 || q_len < 1 || !std::isfinite(scale))
         return PA_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
     if (head_dim != pa::kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
     const int group = num_q_heads / num_kv_heads;
-    const int gp = pa::decode_group_pad(group);
+    if (q_len > 16) return PA_ERR_UNSUPPORTED;
+    const int gp = pa::decode_group_pad(group * q_len);
     if (gp == 0) return PA_ERR_UNSUPPORTED;
     if (num_seqs == 0) return PA_OK;
     if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
@@ -64,7 +66,7 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
         return PA_ERR_INVALID_ARG;
     if (max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_INVALID_ARG;
 
-    const pa::DecodeKernel kind = decode_kernel_choice(gp);
+    const pa::DecodeKernel kind = decode_kernel_choice(gp, q_len);
     const int P = plan_workers(gp, kind, num_partitions);
     if (P <= 0) return PA_ERR_CUDA;
     if (!workspace || !aligned16(workspace) || workspace_bytes < pa::decode_workspace_bytes(gp, P))
@@ -81,6 +83,8 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
     a.num_q_heads = num_q_heads;
     a.num_kv_heads = num_kv_heads;
     a.group = group;
+    a.q_len = q_len;
+    a.cols = group * q_len;
     a.block_size_log2 = log2_exact(block_size);
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = num_blocks;
@@ -147,7 +151,7 @@ pa_status_t pa_decode(const void *q, const void *k_cache, const void *v_cache,
                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                       int64_t num_blocks, void *workspace, size_t workspace_bytes,
                       void *stream) {
-    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
                        scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                        num_blocks, workspace, workspace_bytes, 0, stream);
 }
@@ -159,9 +163,31 @@ pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const void *v_c
                              int64_t num_blocks, void *workspace, size_t workspace_bytes,
                              int num_partitions, void *stream) {
     if (num_partitions < 0) return PA_ERR_INVALID_ARG;
-    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
                        scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                        num_blocks, workspace, workspace_bytes, num_partitions, stream);
+}
+
+size_t pa_decode_multi_workspace_size(int q_len, int num_q_heads, int num_kv_heads,
+                                      int head_dim) {
+    if (q_len < 1 || q_len > 16 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || head_dim != pa::kHeadDimPublic)
+        return 0;
+    const int gp = pa::decode_group_pad(num_q_heads / num_kv_heads * q_len);
+    if (gp == 0) return 0;
+    const int P = plan_workers(gp, pa::DecodeKernel::kMma, 0);
+    return P > 0 ? pa::decode_workspace_bytes(gp, P) : 0;
+}
+
+pa_status_t pa_decode_multi(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int q_len, float scale, void *out,
+                            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       q_len, scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       block_size, num_blocks, workspace, workspace_bytes, 0, stream);
 }
 
 }  // extern "C"

@@ -116,6 +116,22 @@ __device__ __forceinline__ void issue_tile(const Cursor &c, int bid, uint8_t *st
     }
 }
 
+// Element offset of the q (and out) row of column c of a (sequence, KV head)
+// unit. Columns are (query token i, head h of the group) pairs, c = i g + h;
+// single-token decode has one query token, so columns are the group's heads.
+__device__ __forceinline__ int64_t col_row(const DecodeArgs &a, int s, int kvh, int c) {
+    const int g = a.group;
+    const int i = c / g, h = c - i * g;
+    return (((int64_t)s * a.q_len + i) * a.num_q_heads + (int64_t)kvh * g + h) * kHeadDim;
+}
+
+// Tokens column c may see in a sequence of L tokens: query token i of the
+// q_len new ones sits at position L - q_len + i and sees t <= that position.
+__device__ __forceinline__ int col_limit(const DecodeArgs &a, int L, int c) {
+    const int lim = L - a.q_len + c / a.group + 1;
+    return c < a.cols ? (lim > 0 ? lim : 0) : 0;
+}
+
 // ---------------------------------------------------------------------------
 // Tile computation on the tensor cores.
 //
@@ -135,17 +151,22 @@ struct MmaTile {
     uint32_t qb[NT][8][2];
     float o[NT][8][4];
     float m[NT][2], l[NT][2];
+    int lim[NT][2];     // tokens visible to this lane's two score columns per column tile
 
-    __device__ __forceinline__ void begin(const uint16_t *qrow, int g, int lane) {
+    __device__ __forceinline__ void begin(const DecodeArgs &a, const Cursor &cur, int lane) {
         const int gid = lane >> 2, tig = lane & 3;
+        const uint16_t *qg = static_cast<const uint16_t *>(a.q);
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const int h = nt * 8 + gid;
+            const int h = nt * 8 + gid;          // this lane's column of the Q^T operand
+            lim[nt][0] = col_limit(a, cur.L, nt * 8 + 2 * tig);
+            lim[nt][1] = col_limit(a, cur.L, nt * 8 + 2 * tig + 1);
 #pragma unroll
             for (int kk = 0; kk < 8; ++kk) {
                 uint32_t w0 = 0u, w1 = 0u;
-                if (h < g) {
-                    const uint32_t *p = reinterpret_cast<const uint32_t *>(qrow + h * kHeadDim + kk * 16 + tig * 2);
+                if (h < a.cols) {
+                    const uint32_t *p = reinterpret_cast<const uint32_t *>(
+                        qg + col_row(a, cur.s, cur.kvh, h) + kk * 16 + tig * 2);
                     w0 = __ldg(p);
                     w1 = __ldg(p + 4);
                 }
@@ -161,7 +182,7 @@ struct MmaTile {
         }
     }
 
-    __device__ __forceinline__ void tile(const uint8_t *stage, int valid, float scale_log2,
+    __device__ __forceinline__ void tile(const uint8_t *stage, int t0, float scale_log2,
                                          float *, int lane) {
         const uint32_t base = smem_u32(stage);
         const int i7 = lane & 7, mi = lane >> 3;
@@ -181,14 +202,15 @@ struct MmaTile {
             for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(s[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
         }
 
-        const bool ok0 = gid < valid, ok1 = gid + 8 < valid;
+        // token t0 + gid (and + 8) is visible to a column below its limit
+        const int r0 = t0 + gid, r1 = t0 + gid + 8;
         uint32_t pb0[NT], pb1[NT];
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {
-            const float s0 = ok0 ? s[nt][0] * scale_log2 : kNegInf;
-            const float s1 = ok0 ? s[nt][1] * scale_log2 : kNegInf;
-            const float s2 = ok1 ? s[nt][2] * scale_log2 : kNegInf;
-            const float s3 = ok1 ? s[nt][3] * scale_log2 : kNegInf;
+            const float s0 = r0 < lim[nt][0] ? s[nt][0] * scale_log2 : kNegInf;
+            const float s1 = r0 < lim[nt][1] ? s[nt][1] * scale_log2 : kNegInf;
+            const float s2 = r1 < lim[nt][0] ? s[nt][2] * scale_log2 : kNegInf;
+            const float s3 = r1 < lim[nt][1] ? s[nt][3] * scale_log2 : kNegInf;
             float mx0 = fmaxf(s0, s2), mx1 = fmaxf(s1, s3);
 #pragma unroll
             for (int x = 4; x <= 16; x <<= 1) {
@@ -308,13 +330,16 @@ struct SimtTile {
     static constexpr bool kSwizzle = false;
     static constexpr int kScratchFloats = 16 * GP + GP;  // p[16][GP], alpha[GP]
     float qf[GP][4], o[GP][4], m_run[HP], l_run[HP];
-    float scale_log2_;
+    int L_;             // tokens of the unit's sequence (one query token per sequence)
 
-    __device__ __forceinline__ void begin(const uint16_t *qrow, int g, int lane) {
+    __device__ __forceinline__ void begin(const DecodeArgs &a, const Cursor &cur, int lane) {
+        const uint16_t *qg = static_cast<const uint16_t *>(a.q);
+        L_ = cur.L;
 #pragma unroll
         for (int h = 0; h < GP; ++h) {
             uint2 u = make_uint2(0u, 0u);
-            if (h < g) u = __ldg(reinterpret_cast<const uint2 *>(qrow + h * kHeadDim) + lane);
+            if (h < a.cols)
+                u = __ldg(reinterpret_cast<const uint2 *>(qg + col_row(a, cur.s, cur.kvh, h)) + lane);
             qf[h][0] = bf16_lo(u.x);
             qf[h][1] = bf16_hi(u.x);
             qf[h][2] = bf16_lo(u.y);
@@ -329,8 +354,9 @@ struct SimtTile {
         }
     }
 
-    __device__ __forceinline__ void tile(const uint8_t *stage, int valid, float scale_log2,
+    __device__ __forceinline__ void tile(const uint8_t *stage, int t0, float scale_log2,
                                          float *scratch, int lane) {
+        const int valid = L_ - t0 < 0 ? 0 : (L_ - t0 > 16 ? 16 : L_ - t0);
         const uint8_t *sk = stage;
         const uint8_t *sv = stage + kTileBytes;
         float *sp = scratch;              // p[16][GP]
@@ -546,8 +572,6 @@ decode_kernel(const DecodeArgs a) {
         return;
     }
 
-    const int g = a.group;
-    const uint16_t *qg = static_cast<const uint16_t *>(a.q);
     uint32_t *outg = static_cast<uint32_t *>(a.out);
 
     // producer: runs kStages - 1 tiles ahead of the consumer
@@ -589,13 +613,13 @@ decode_kernel(const DecodeArgs a) {
             fresh = false;
             piece_T = T;
             piece_j0 = cc.j;
-            tl.begin(qg + ((int64_t)cc.s * a.num_q_heads + (int64_t)cc.kvh * g) * kHeadDim, g, lane);
+            tl.begin(a, cc, lane);
         }
 
         cp_async_wait<kStages - 1>();
         __syncwarp();
         uint8_t *stage = ring + stage_c * kStageBytes;
-        tl.tile(stage, tile_valid(cc), a.scale_log2, scratch, lane);
+        tl.tile(stage, cc.j << 4, a.scale_log2, scratch, lane);
         stage_c = stage_c + 1 == kStages ? 0 : stage_c + 1;
 
         const bool unit_end = cc.j == cc.nt - 1;
@@ -608,16 +632,15 @@ decode_kernel(const DecodeArgs a) {
             __syncwarp();
             if (piece_j0 == 0 && unit_end) {
                 // the whole unit is in this share: normalise and write bf16
-                uint32_t *orow = outg + (((int64_t)cc.s * a.num_q_heads + (int64_t)cc.kvh * g) * kHeadDim) / 2;
 #pragma unroll
                 for (int h = 0; h < GP; ++h) {
-                    if (h < g) {
+                    if (h < a.cols) {
                         const float l = sm_l[h];
                         const float inv = l > 0.f ? 1.f / l : 0.f;
                         uint2 pk;
                         pk.x = pack_bf16x2(oc[h][0] * inv, oc[h][1] * inv);
                         pk.y = pack_bf16x2(oc[h][2] * inv, oc[h][3] * inv);
-                        reinterpret_cast<uint2 *>(orow + h * (kHeadDim / 2))[lane] = pk;
+                        reinterpret_cast<uint2 *>(outg + col_row(a, cc.s, cc.kvh, h) / 2)[lane] = pk;
                     }
                 }
             } else {
@@ -649,7 +672,7 @@ decode_kernel(const DecodeArgs a) {
 }
 
 // Log-sum-exp merge of the pieces of each split unit. One warp per worker's
-// task; lane l handles dims [4l, 4l + 4) of each query head.
+// task; lane l handles dims [4l, 4l + 4) of each column.
 template <int GP>
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     // programmatic dependent of the decode grid: wait for all of it (and its
@@ -661,11 +684,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     const int4 task = a.tasks[w];
     if (task.x < 0) return;
     const int n = 1 + task.w - w;
-    const int g = a.group;
     const float2 *ml = reinterpret_cast<const float2 *>(a.part_ml);
-    uint32_t *orow = static_cast<uint32_t *>(a.out) +
-                     (((int64_t)task.x * a.num_q_heads + (int64_t)task.y * g) * kHeadDim) / 2;
-    for (int h = 0; h < g; ++h) {
+    uint32_t *outg = static_cast<uint32_t *>(a.out);
+    for (int h = 0; h < a.cols; ++h) {
         float M = kNegInf;
         for (int i = 0; i < n; ++i) {
             const int slot = i == 0 ? task.z : 2 * (w + i);
@@ -687,7 +708,7 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
         uint2 pk;
         pk.x = pack_bf16x2(acc0 * inv, acc1 * inv);
         pk.y = pack_bf16x2(acc2 * inv, acc3 * inv);
-        reinterpret_cast<uint2 *>(orow + h * (kHeadDim / 2))[lane] = pk;
+        reinterpret_cast<uint2 *>(outg + col_row(a, task.x, task.y, h) / 2)[lane] = pk;
     }
 }
 

@@ -28,6 +28,8 @@ struct DecodeArgs {
     int num_q_heads;
     int num_kv_heads;
     int group;                  // Hq / Hkv
+    int q_len;                  // query tokens per sequence (1: plain decode)
+    int cols;                   // q_len * group: (query token, head) columns per KV head
     int block_size_log2;
     int max_blocks_per_seq;
     int64_t num_blocks;

@@ -31,6 +31,9 @@ SIGNATURES = {
                           _I64, _P, _SZ, _I32, _P], _I32),
     "pa_decode_noalloc": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                            _I64, _P], _I32),
+    "pa_decode_multi_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
+    "pa_decode_multi": ([_P, _P, _P, _P, _I32, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32, _I32,
+                         _I64, _P, _SZ, _P], _I32),
 }
 
 _lock = threading.Lock()
@@ -175,6 +178,50 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
         else:
             st = lib().pa_decode(*args, _stream_ptr(stream, dev))
     _check("pa_decode", st)
+    return out
+
+
+def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
+                 workspace=None, stream=None):
+    """Decode of Q new tokens per sequence (speculative verification): q is
+    bf16 [S, Q, Hq, D]; query token i attends to keys t <= L - Q + i, with
+    L = context_lens[s] counting all Q new tokens. Returns out [S, Q, Hq, D]."""
+    dev = q.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                     (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
+                     (context_lens, "context_lens", torch.int32)):
+        _cuda(t, n, dt, dev)
+    S, Q, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    if v_cache.shape != k_cache.shape or D2 != D or block_tables.dim() != 2 \
+            or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("shape mismatch between q, caches, block_tables and context_lens")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda(out, "out", torch.bfloat16, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if workspace is None:
+        with torch.cuda.device(dev):
+            n = lib().pa_decode_multi_workspace_size(Q, Hq, Hkv, D)
+        if n == 0:
+            raise ValueError("unsupported query-token / head configuration")
+        key = (dev, "multi", n)
+        workspace = _workspaces.get(key)
+        if workspace is None:
+            workspace = torch.zeros(n, dtype=torch.uint8, device=dev)
+            _workspaces[key] = workspace
+    else:
+        _cuda(workspace, "workspace", workspace.dtype, dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        st = lib().pa_decode_multi(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                   block_tables.data_ptr(), block_tables.shape[1],
+                                   context_lens.data_ptr(), Q, float(scale), out.data_ptr(), S,
+                                   Hq, Hkv, D, bs, NB, workspace.data_ptr(), ws_bytes,
+                                   _stream_ptr(stream, dev))
+    _check("pa_decode_multi", st)
     return out
 
 
