@@ -671,8 +671,10 @@ decode_kernel(const DecodeArgs a) {
     if (lane == 0) a.tasks[w] = task;
 }
 
-// Log-sum-exp merge of the pieces of each split unit. One warp per worker's
-// task; lane l handles dims [4l, 4l + 4) of each column.
+// Log-sum-exp merge of the pieces of each split unit. Block (x, y) holds
+// four warps, one per worker task 4x .. 4x + 3, all on column y; lane l
+// handles dims [4l, 4l + 4). One online pass over the pieces: each piece's
+// (max, sum, o) is folded in with weights 2^(m_i - M).
 template <int GP>
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     // programmatic dependent of the decode grid: wait for all of it (and its
@@ -680,36 +682,33 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     asm volatile("griddepcontrol.wait;\n" ::: "memory");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int w = blockIdx.x * 4 + warp;
-    if (w >= a.num_workers) return;
+    const int h = blockIdx.y;
+    if (w >= a.num_workers || h >= a.cols) return;
     const int4 task = a.tasks[w];
     if (task.x < 0) return;
     const int n = 1 + task.w - w;
     const float2 *ml = reinterpret_cast<const float2 *>(a.part_ml);
-    uint32_t *outg = static_cast<uint32_t *>(a.out);
-    for (int h = 0; h < a.cols; ++h) {
-        float M = kNegInf;
-        for (int i = 0; i < n; ++i) {
-            const int slot = i == 0 ? task.z : 2 * (w + i);
-            M = fmaxf(M, ml[(int64_t)slot * GP + h].x);
-        }
-        float L = 0.f, acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-        for (int i = 0; i < n; ++i) {
-            const int slot = i == 0 ? task.z : 2 * (w + i);
-            const float2 e = ml[(int64_t)slot * GP + h];
-            const float wt = ex2(e.x - M);
-            L = fmaf(wt, e.y, L);
-            const float4 po = reinterpret_cast<const float4 *>(a.part_o + ((int64_t)slot * GP + h) * kHeadDim)[lane];
-            acc0 = fmaf(wt, po.x, acc0);
-            acc1 = fmaf(wt, po.y, acc1);
-            acc2 = fmaf(wt, po.z, acc2);
-            acc3 = fmaf(wt, po.w, acc3);
-        }
-        const float inv = L > 0.f ? 1.f / L : 0.f;
-        uint2 pk;
-        pk.x = pack_bf16x2(acc0 * inv, acc1 * inv);
-        pk.y = pack_bf16x2(acc2 * inv, acc3 * inv);
-        reinterpret_cast<uint2 *>(outg + col_row(a, task.x, task.y, h) / 2)[lane] = pk;
+    float M = kNegInf, L = 0.f, acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
+#pragma unroll 4
+    for (int i = 0; i < n; ++i) {
+        const int slot = i == 0 ? task.z : 2 * (w + i);
+        const float2 e = ml[(int64_t)slot * GP + h];
+        const float4 po = reinterpret_cast<const float4 *>(a.part_o + ((int64_t)slot * GP + h) * kHeadDim)[lane];
+        if (e.x == kNegInf) continue;        // no visible token of this column in the piece
+        const float Mn = fmaxf(M, e.x);
+        const float a_old = ex2(M - Mn), a_new = ex2(e.x - Mn);
+        L = L * a_old + e.y * a_new;
+        acc0 = acc0 * a_old + po.x * a_new;
+        acc1 = acc1 * a_old + po.y * a_new;
+        acc2 = acc2 * a_old + po.z * a_new;
+        acc3 = acc3 * a_old + po.w * a_new;
+        M = Mn;
     }
+    const float inv = L > 0.f ? 1.f / L : 0.f;
+    uint2 pk;
+    pk.x = pack_bf16x2(acc0 * inv, acc1 * inv);
+    pk.y = pack_bf16x2(acc2 * inv, acc3 * inv);
+    reinterpret_cast<uint2 *>(static_cast<uint32_t *>(a.out) + col_row(a, task.x, task.y, h) / 2)[lane] = pk;
 }
 
 template <class Tile, int GP>
@@ -730,10 +729,10 @@ struct Launcher {
     // Both kernels go out as programmatic dependent launches: each may be
     // scheduled while the kernel before it in the stream is still running, and
     // waits for it (griddepcontrol.wait) before touching its results.
-    static cudaError_t launch_pdl(const void *fn, unsigned grid, unsigned block, size_t smem,
+    static cudaError_t launch_pdl(const void *fn, dim3 grid, unsigned block, size_t smem,
                                   const DecodeArgs &a, cudaStream_t st) {
         cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3(grid);
+        cfg.gridDim = grid;
         cfg.blockDim = dim3(block);
         cfg.dynamicSmemBytes = smem;
         cfg.stream = st;
@@ -749,11 +748,11 @@ struct Launcher {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
         const unsigned grid = (a.num_workers + kWarps - 1) / kWarps;
-        e = launch_pdl(reinterpret_cast<const void *>(&decode_kernel<Tile, GP>), grid,
+        e = launch_pdl(reinterpret_cast<const void *>(&decode_kernel<Tile, GP>), dim3(grid),
                        kWarps * 32, Lay::kCtaBytes, a, st);
         if (e != cudaSuccess) return e;
         e = launch_pdl(reinterpret_cast<const void *>(&combine_kernel<GP>),
-                       (a.num_workers + 3) / 4, 128, 0, a, st);
+                       dim3((a.num_workers + 3) / 4, a.cols), 128, 0, a, st);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }
