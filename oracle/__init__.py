@@ -85,6 +85,11 @@ class Oracle:
         lib.oracle_decode_multi.argtypes = [p, p, p, p, i32, p, i32, dbl, p, i32, i32, i32, i32,
                                             i32, i64, i32]
         lib.oracle_decode_multi.restype = i32
+        lib.oracle_store_kvcache_layout.argtypes = [p, p, p, p, p, i64, i32, i32, i32, i64, i32]
+        lib.oracle_store_kvcache_layout.restype = i32
+        lib.oracle_decode_layout.argtypes = [p, p, p, p, i32, p, dbl, p, i32, i32, i32, i32, i32,
+                                             i64, i32, i32]
+        lib.oracle_decode_layout.restype = i32
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         self.lib = lib
@@ -158,6 +163,35 @@ class Oracle:
             raise OracleError(f"oracle_decode_pairs returned {rc}")
         return out
 
+
+    def store_kvcache_head_major(self, k, v, k_cache, v_cache, slot_mapping):
+        """The store into a head-major pool [NB, Hkv, bs, D]; returns new
+        (k_cache, v_cache) uint16 arrays."""
+        kb, vb = _bits(k), _bits(v)
+        kc, vc = _bits(k_cache).copy(), _bits(v_cache).copy()
+        sm = _arr(slot_mapping, np.int64)
+        NB, Hkv, bs, D = kc.shape
+        rc = self.lib.oracle_store_kvcache_layout(_ptr(kb), _ptr(vb), _ptr(kc), _ptr(vc),
+                                                  _ptr(sm), sm.shape[0], Hkv, D, bs, NB, 1)
+        if rc != OK:
+            raise OracleError(f"oracle_store_kvcache_layout returned {rc}")
+        return kc, vc
+
+    def decode_head_major(self, q, k_cache, v_cache, block_tables, context_lens, scale,
+                          threads: int = 0):
+        """fp64 [S, Hq, D] decode over a head-major pool [NB, Hkv, bs, D]."""
+        qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+        bt = _arr(block_tables, np.int32)
+        cl = _arr(context_lens, np.int32)
+        S, Hq, D = qb.shape
+        NB, Hkv, bs, _ = kc.shape
+        out = np.zeros((S, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_decode_layout(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                                           _ptr(cl), float(scale), _ptr(out), S, Hq, Hkv, D, bs,
+                                           NB, 1, int(threads))
+        if rc != OK:
+            raise OracleError(f"oracle_decode_layout returned {rc}")
+        return out
 
     def decode_multi(self, q, k_cache, v_cache, block_tables, context_lens, scale,
                      threads: int = 0):

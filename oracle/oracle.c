@@ -53,11 +53,11 @@ static double bf16_to_double(uint16_t x)
     return (double)f;
 }
 
-int oracle_store_kvcache(const uint16_t *k, const uint16_t *v,
-                         uint16_t *k_cache, uint16_t *v_cache,
-                         const int64_t *slot_mapping, int64_t num_tokens,
-                         int num_kv_heads, int head_dim, int block_size,
-                         int64_t num_blocks)
+int oracle_store_kvcache_layout(const uint16_t *k, const uint16_t *v,
+                                uint16_t *k_cache, uint16_t *v_cache,
+                                const int64_t *slot_mapping, int64_t num_tokens,
+                                int num_kv_heads, int head_dim, int block_size,
+                                int64_t num_blocks, int layout)
 {
     if (num_tokens < 0 || num_kv_heads <= 0 || head_dim <= 0 || block_size <= 0 || num_blocks < 0)
         return ORACLE_ERR_ARG;
@@ -73,10 +73,33 @@ int oracle_store_kvcache(const uint16_t *k, const uint16_t *v,
         int64_t slot = slot_mapping[i];
         if (slot == -1)
             continue; /* padding entry: nothing is written */
+        if (layout == ORACLE_LAYOUT_HEAD_MAJOR) {
+            /* [block][kv head][offset]: the row's heads land block_size rows apart */
+            const int64_t block = slot / block_size, off = slot % block_size;
+            for (int h = 0; h < num_kv_heads; ++h) {
+                const int64_t dst = ((block * num_kv_heads + h) * block_size + off) * head_dim;
+                memcpy(k_cache + dst, k + i * row + (int64_t)h * head_dim,
+                       (size_t)head_dim * sizeof(uint16_t));
+                memcpy(v_cache + dst, v + i * row + (int64_t)h * head_dim,
+                       (size_t)head_dim * sizeof(uint16_t));
+            }
+            continue;
+        }
         memcpy(k_cache + slot * row, k + i * row, (size_t)row * sizeof(uint16_t));
         memcpy(v_cache + slot * row, v + i * row, (size_t)row * sizeof(uint16_t));
     }
     return ORACLE_OK;
+}
+
+int oracle_store_kvcache(const uint16_t *k, const uint16_t *v,
+                         uint16_t *k_cache, uint16_t *v_cache,
+                         const int64_t *slot_mapping, int64_t num_tokens,
+                         int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks)
+{
+    return oracle_store_kvcache_layout(k, v, k_cache, v_cache, slot_mapping, num_tokens,
+                                       num_kv_heads, head_dim, block_size, num_blocks,
+                                       ORACLE_LAYOUT_TOKEN_MAJOR);
 }
 
 /* One output row: query head h of query row q_index, attending to the first
@@ -86,7 +109,8 @@ static int decode_one(const uint16_t *q, const uint16_t *k_cache, const uint16_t
                       const int32_t *block_tables, int max_blocks_per_seq,
                       const int32_t *context_lens, double scale,
                       int s, int h, int num_q_heads, int num_kv_heads, int head_dim,
-                      int block_size, int64_t num_blocks, int q_index, int cap, double *out)
+                      int block_size, int64_t num_blocks, int q_index, int cap, int layout,
+                      double *out)
 {
     const int group = num_q_heads / num_kv_heads;
     const int kvh = h / group;
@@ -112,8 +136,9 @@ static int decode_one(const uint16_t *q, const uint16_t *k_cache, const uint16_t
             free(score);
             return ORACLE_ERR_RANGE;
         }
-        const uint16_t *krow = k_cache +
-            ((block * block_size + t % block_size) * num_kv_heads + kvh) * (int64_t)head_dim;
+        const uint16_t *krow = layout == ORACLE_LAYOUT_HEAD_MAJOR
+            ? k_cache + ((block * num_kv_heads + kvh) * block_size + t % block_size) * (int64_t)head_dim
+            : k_cache + ((block * block_size + t % block_size) * num_kv_heads + kvh) * (int64_t)head_dim;
         double dot = 0.0;
         for (int d = 0; d < head_dim; ++d)
             dot += bf16_to_double(qrow[d]) * bf16_to_double(krow[d]);
@@ -134,8 +159,9 @@ static int decode_one(const uint16_t *q, const uint16_t *k_cache, const uint16_t
     /* out = sum_t p_t V_t, V_t gathered the same way as K_t */
     for (int t = 0; t < L; ++t) {
         int64_t block = block_tables[(int64_t)s * max_blocks_per_seq + t / block_size];
-        const uint16_t *vrow = v_cache +
-            ((block * block_size + t % block_size) * num_kv_heads + kvh) * (int64_t)head_dim;
+        const uint16_t *vrow = layout == ORACLE_LAYOUT_HEAD_MAJOR
+            ? v_cache + ((block * num_kv_heads + kvh) * block_size + t % block_size) * (int64_t)head_dim
+            : v_cache + ((block * block_size + t % block_size) * num_kv_heads + kvh) * (int64_t)head_dim;
         double p = score[t] / denom;
         for (int d = 0; d < head_dim; ++d)
             out[d] += p * bf16_to_double(vrow[d]);
@@ -153,11 +179,11 @@ static int check_shape(int num_seqs, int num_q_heads, int num_kv_heads, int head
     return ORACLE_OK;
 }
 
-int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
-                  const int32_t *block_tables, int max_blocks_per_seq,
-                  const int32_t *context_lens, double scale, double *out,
-                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                  int block_size, int64_t num_blocks, int num_threads)
+int oracle_decode_layout(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, double scale, double *out,
+                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int64_t num_blocks, int layout, int num_threads)
 {
     int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                          max_blocks_per_seq);
@@ -174,7 +200,7 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
         const int s = (int)(i / num_q_heads);
         int r = decode_one(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            scale, s, (int)(i % num_q_heads), num_q_heads, num_kv_heads,
-                           head_dim, block_size, num_blocks, s, context_lens[s],
+                           head_dim, block_size, num_blocks, s, context_lens[s], layout,
                            out + i * head_dim);
         if (r != ORACLE_OK) {
 #ifdef _OPENMP
@@ -185,6 +211,18 @@ int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_
     }
     (void)num_threads;
     return err;
+}
+
+int oracle_decode(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                  const int32_t *block_tables, int max_blocks_per_seq,
+                  const int32_t *context_lens, double scale, double *out,
+                  int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                  int block_size, int64_t num_blocks, int num_threads)
+{
+    return oracle_decode_layout(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, scale, out, num_seqs, num_q_heads, num_kv_heads,
+                                head_dim, block_size, num_blocks, ORACLE_LAYOUT_TOKEN_MAJOR,
+                                num_threads);
 }
 
 int oracle_decode_pairs(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
@@ -212,7 +250,8 @@ int oracle_decode_pairs(const uint16_t *q, const uint16_t *k_cache, const uint16
         int r = decode_one(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            scale, pairs[2 * i], pairs[2 * i + 1], num_q_heads, num_kv_heads,
                            head_dim, block_size, num_blocks, pairs[2 * i],
-                           context_lens[pairs[2 * i]], out + i * head_dim);
+                           context_lens[pairs[2 * i]], ORACLE_LAYOUT_TOKEN_MAJOR,
+                           out + i * head_dim);
         if (r != ORACLE_OK) {
 #ifdef _OPENMP
 #pragma omp critical
@@ -259,7 +298,7 @@ int oracle_decode_multi(const uint16_t *q, const uint16_t *k_cache, const uint16
         int r = decode_one(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                            scale, s, (int)(r_i % num_q_heads), num_q_heads, num_kv_heads,
                            head_dim, block_size, num_blocks, (int)row, cap,
-                           out + r_i * head_dim);
+                           ORACLE_LAYOUT_TOKEN_MAJOR, out + r_i * head_dim);
         if (r != ORACLE_OK) {
 #ifdef _OPENMP
 #pragma omp critical

@@ -24,6 +24,10 @@ extern "C" {
 
 enum { ORACLE_OK = 0, ORACLE_ERR_ARG = 1, ORACLE_ERR_RANGE = 2 };
 
+/* Pool layouts: token-major [num_blocks][block_size][num_kv_heads][head_dim]
+ * (the default), head-major [num_blocks][num_kv_heads][block_size][head_dim]. */
+enum { ORACLE_LAYOUT_TOKEN_MAJOR = 0, ORACLE_LAYOUT_HEAD_MAJOR = 1 };
+
 /* Copy row i of k and v to cache slot slot_mapping[i]; -1 rows are skipped.
  * Nothing is written if any slot is out of range. */
 int oracle_store_kvcache(const uint16_t *k, const uint16_t *v,
@@ -58,6 +62,18 @@ int oracle_decode_multi(const uint16_t *q, const uint16_t *k_cache, const uint16
                         const int32_t *context_lens, int q_len, double scale, double *out,
                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                         int block_size, int64_t num_blocks, int num_threads);
+
+/* The store and decode above for a pool in either layout. */
+int oracle_store_kvcache_layout(const uint16_t *k, const uint16_t *v,
+                                uint16_t *k_cache, uint16_t *v_cache,
+                                const int64_t *slot_mapping, int64_t num_tokens,
+                                int num_kv_heads, int head_dim, int block_size,
+                                int64_t num_blocks, int layout);
+int oracle_decode_layout(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, double scale, double *out,
+                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                         int block_size, int64_t num_blocks, int layout, int num_threads);
 
 /* Threads the OpenMP loops use by default. */
 int oracle_num_threads(void);

@@ -326,6 +326,26 @@ def pin_multi_prefix(O):
         assert np.array_equal(out[:, i], single), f"query token {i}"
 
 
+def _head_major(pool):
+    return pool.permute(0, 2, 1, 3).contiguous()
+
+
+def pin_head_major(O):
+    """The head-major pool [NB, Hkv, bs, D] is the token-major one with two
+    axes swapped: its store and decode give the same values, bit for bit."""
+    for spec in (inputs.SPECS["tiny"],
+                 inputs.scaled(inputs.SPECS["prefix_shared"], num_seqs=6, ctx_div=8, name="ps")):
+        wl = inputs.generate(spec, seed=51)
+        kc, vc = O.store_kvcache(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping)
+        hk, hv = O.store_kvcache_head_major(wl.k_new, wl.v_new, _head_major(wl.k_cache),
+                                            _head_major(wl.v_cache), wl.slot_mapping)
+        assert np.array_equal(hk, np.ascontiguousarray(kc.transpose(0, 2, 1, 3))), "head-major store"
+        assert np.array_equal(hv, np.ascontiguousarray(vc.transpose(0, 2, 1, 3))), "head-major store"
+        a = O.decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+        b = O.decode_head_major(wl.q, hk, hv, wl.block_tables, wl.context_lens, wl.scale)
+        assert np.array_equal(a, b), "head-major decode"
+
+
 ALL_PINS = [pin_sdpa, pin_single_token, pin_zero_keys, pin_unit_values, pin_three_tokens,
             pin_dominant_key, pin_renumbering, pin_prefix_private, pin_block_size,
-            pin_nan_free, pin_store, pin_multi_sdpa, pin_multi_prefix]
+            pin_nan_free, pin_store, pin_multi_sdpa, pin_multi_prefix, pin_head_major]

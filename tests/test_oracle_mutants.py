@@ -28,6 +28,11 @@ MUTANTS = [
      "const int cap = context_lens[s];"),
     ("store_v_from_k", "memcpy(v_cache + slot * row, v + i * row",
      "memcpy(v_cache + slot * row, k + i * row"),
+    ("head_major_rows_token_major",
+     "? k_cache + ((block * num_kv_heads + kvh) * block_size + t % block_size) * (int64_t)head_dim",
+     "? k_cache + ((block * block_size + t % block_size) * num_kv_heads + kvh) * (int64_t)head_dim"),
+    ("head_major_store_head_stride", "const int64_t dst = ((block * num_kv_heads + h) * block_size + off) * head_dim;",
+     "const int64_t dst = ((block * block_size + off) * num_kv_heads + h) * head_dim;"),
     ("store_skips_first_row", "if (slot == -1)\n            continue;",
      "if (slot == -1 || i == 0)\n            continue;"),
 ]
