@@ -246,6 +246,12 @@ def run_gpu(args, rank, world, local):
     S, Hq, Hkv, D = wl.num_seqs, wl.spec.num_q_heads, wl.spec.num_kv_heads, wl.spec.head_dim
     q = wl.q
     k_cache, v_cache = wl.k_cache, wl.v_cache
+    HM = args.layout == "head_major"
+    if HM:          # the same values in a [NB, Hkv, bs, D] pool
+        k_cache = k_cache.permute(0, 2, 1, 3).contiguous()
+        v_cache = v_cache.permute(0, 2, 1, 3).contiguous()
+        if args.q_len > 1:
+            raise SystemExit("--q-len > 1 runs on the token-major layout only")
     k_new, v_new = wl.k_new, wl.v_new
     slots = torch.from_numpy(wl.slot_mapping).to(dev)
     bt = torch.from_numpy(wl.block_tables).to(dev)
@@ -262,14 +268,15 @@ def run_gpu(args, rank, world, local):
     def decode_call(q_, bt_, cl_):
         if Q > 1:
             return pa.decode_multi(q_, k_cache, v_cache, bt_, cl_, wl.scale, out=out)
-        return pa.decode(q_, k_cache, v_cache, bt_, cl_, wl.scale, out=out, workspace=ws)
+        return pa.decode(q_, k_cache, v_cache, bt_, cl_, wl.scale, out=out, workspace=ws,
+                         head_major=HM)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
     has_store = slots.shape[0] > 0
 
     def step():
         if has_store:
-            pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots)
+            pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots, head_major=HM)
         decode_call(q, bt, cl)
 
     # ---- device-resident timing: store then decode back to back, as a user
@@ -301,7 +308,7 @@ def run_gpu(args, rank, world, local):
         flush.zero_()
         ev[i][0].record(stream)
         if has_store:
-            pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots)
+            pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots, head_major=HM)
         ev[i][1].record(stream)
         decode_call(q, bt, cl)
         ev[i][2].record(stream)
@@ -333,7 +340,7 @@ def run_gpu(args, rank, world, local):
     def e2e_step():
         d_stage.copy_(h_stage, non_blocking=True)
         if has_store:
-            pa.store_kvcache(dk, dv, k_cache, v_cache, ds)
+            pa.store_kvcache(dk, dv, k_cache, v_cache, ds, head_major=HM)
         decode_call(dq, dbt, dcl)
         hout.copy_(out, non_blocking=True)
 
@@ -374,11 +381,13 @@ def run_gpu(args, rank, world, local):
 
     def time_graphs():
         g_dev = pa.DecodeStepGraph(q, k_cache, v_cache, bt, cl, wl.scale, k_new=k_new, v_new=v_new,
-                                   slot_mapping=slots if has_store else None, out=out)
+                                   slot_mapping=slots if has_store else None, out=out,
+                                   head_major=HM)
         graph_ms = time_replay(g_dev)
         g_e2e = pa.DecodeStepGraph(dq, k_cache, v_cache, dbt, dcl, wl.scale, k_new=dk, v_new=dv,
                                    slot_mapping=ds if has_store else None, out=out,
-                                   host_stage=h_stage, device_stage=d_stage, host_out=hout)
+                                   host_stage=h_stage, device_stage=d_stage, host_out=hout,
+                                   head_major=HM)
         graph_e2e_ms = time_replay(g_e2e)
         torch.cuda.synchronize()
         if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
@@ -398,7 +407,7 @@ def run_gpu(args, rank, world, local):
         "metric": METRIC, "value": ms * 1e3, "unit": "us/step", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": dict(workload_config(wl), q_len=Q),
+        "data": "synthetic", "config": dict(workload_config(wl), q_len=Q, layout=args.layout),
         "store_us": store_avg * 1e3, "decode_us": dec_avg * 1e3,
         "kv_read_gbs": achieved, "hbm_frac": achieved / peak,
         "unique_kv_read_gbs": wl.unique_kv_bytes() / (dec_avg * 1e-3) / 1e9,
@@ -434,6 +443,8 @@ def main():
                     help="run a copy of the workload with this many sequences (profiling)")
     ap.add_argument("--q-len", type=int, default=1,
                     help="query tokens per sequence (speculative verification); 1 = decode")
+    ap.add_argument("--layout", default="token_major", choices=["token_major", "head_major"],
+                    help="KV pool layout: [NB, bs, Hkv, D] or [NB, Hkv, bs, D]")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--cpu-seconds", type=float, default=15.0)
     ap.add_argument("--ref-seconds", type=float, default=60.0)

@@ -64,6 +64,13 @@ typedef enum {
     PA_ERR_CUDA = 4           /* a CUDA call or launch failed              */
 } pa_status_t;
 
+/* KV pool layouts. Token-major is the default of every call that takes no
+ * layout argument. */
+typedef enum {
+    PA_LAYOUT_TOKEN_MAJOR = 0,  /* [num_blocks, block_size, num_kv_heads, head_dim] */
+    PA_LAYOUT_HEAD_MAJOR = 1    /* [num_blocks, num_kv_heads, block_size, head_dim] */
+} pa_layout_t;
+
 /* Human-readable name of a status. Never NULL. */
 PA_API const char *pa_status_string(pa_status_t status);
 
@@ -203,6 +210,30 @@ PA_API pa_status_t pa_decode_multi(const void *q, const void *k_cache, const voi
                                    void *out, int num_seqs, int num_q_heads, int num_kv_heads,
                                    int head_dim, int block_size, int64_t num_blocks,
                                    void *workspace, size_t workspace_bytes, void *stream);
+
+/*
+ * pa_store_kvcache and pa_decode_splitk for a pool in either layout. In the
+ * head-major layout a block keeps each KV head's block_size rows together,
+ * so a 16-token K (or V) tile of one head is one contiguous 4 KB run instead
+ * of 16 rows of 256 B spread num_kv_heads rows apart; slots and block tables
+ * mean the same in both layouts (slot = block * block_size + offset), and the
+ * results are identical. num_partitions = 0 chooses the share count from the
+ * device, as pa_decode. The pages fix no layout; the token-major one is the
+ * plainest reading of a slot_mapping store, the head-major one is offered for
+ * its contiguous tiles.
+ */
+PA_API pa_status_t pa_store_kvcache_layout(const void *k, const void *v,
+                                           void *k_cache, void *v_cache,
+                                           const int64_t *slot_mapping, int64_t num_tokens,
+                                           int num_kv_heads, int head_dim, int block_size,
+                                           int64_t num_blocks, pa_layout_t layout, void *stream);
+PA_API pa_status_t pa_decode_layout(const void *q, const void *k_cache, const void *v_cache,
+                                    const int32_t *block_tables, int max_blocks_per_seq,
+                                    const int32_t *context_lens, float scale, void *out,
+                                    int num_seqs, int num_q_heads, int num_kv_heads,
+                                    int head_dim, int block_size, int64_t num_blocks,
+                                    pa_layout_t layout, void *workspace, size_t workspace_bytes,
+                                    int num_partitions, void *stream);
 
 #ifdef __cplusplus
 }

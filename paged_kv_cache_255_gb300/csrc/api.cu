@@ -48,12 +48,13 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
                         const int32_t *block_tables, int max_blocks_per_seq,
                         const int32_t *context_lens, int q_len, float scale, void *out,
                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                        int block_size, int64_t num_blocks, void *workspace,
+                        int block_size, int64_t num_blocks, int layout, void *workspace,
                         size_t workspace_bytes, int num_partitions, void *stream) {
     if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 ||
         max_blocks_per_seq < 0 || num_partitions < 0 || q_len < 1 || !std::isfinite(scale))
         return PA_ERR_INVALID_ARG;
     if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (layout != PA_LAYOUT_TOKEN_MAJOR && layout != PA_LAYOUT_HEAD_MAJOR) return PA_ERR_INVALID_ARG;
     if (head_dim != pa::kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
     const int group = num_q_heads / num_kv_heads;
     if (q_len > 16) return PA_ERR_UNSUPPORTED;
@@ -86,6 +87,7 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
     a.q_len = q_len;
     a.cols = group * q_len;
     a.block_size_log2 = log2_exact(block_size);
+    a.head_major = layout == PA_LAYOUT_HEAD_MAJOR ? 1 : 0;
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = num_blocks;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);   // scale * log2(e)
@@ -111,10 +113,12 @@ const char *pa_status_string(pa_status_t status) {
     return "PA_ERR_UNKNOWN";
 }
 
-pa_status_t pa_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
-                             const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
-                             int head_dim, int block_size, int64_t num_blocks, void *stream) {
+pa_status_t pa_store_kvcache_layout(const void *k, const void *v, void *k_cache, void *v_cache,
+                                    const int64_t *slot_mapping, int64_t num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int64_t num_blocks, pa_layout_t layout, void *stream) {
     if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (layout != PA_LAYOUT_TOKEN_MAJOR && layout != PA_LAYOUT_HEAD_MAJOR) return PA_ERR_INVALID_ARG;
     if (head_dim != pa::kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
     if (num_tokens == 0) return PA_OK;
     if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
@@ -123,9 +127,18 @@ pa_status_t pa_store_kvcache(const void *k, const void *v, void *k_cache, void *
     const int sms = current_sm_count();
     if (sms <= 0) return PA_ERR_CUDA;
     const cudaError_t e = pa::launch_store_kvcache(
-        k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads * head_dim,
-        num_blocks * block_size, sms, static_cast<cudaStream_t>(stream));
+        k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim,
+        log2_exact(block_size), num_blocks * block_size, layout == PA_LAYOUT_HEAD_MAJOR ? 1 : 0,
+        sms, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status_t pa_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
+                             const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, void *stream) {
+    return pa_store_kvcache_layout(k, v, k_cache, v_cache, slot_mapping, num_tokens,
+                                   num_kv_heads, head_dim, block_size, num_blocks,
+                                   PA_LAYOUT_TOKEN_MAJOR, stream);
 }
 
 size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
@@ -153,7 +166,7 @@ pa_status_t pa_decode(const void *q, const void *k_cache, const void *v_cache,
                       void *stream) {
     return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
                        scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       num_blocks, workspace, workspace_bytes, 0, stream);
+                       num_blocks, PA_LAYOUT_TOKEN_MAJOR, workspace, workspace_bytes, 0, stream);
 }
 
 pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const void *v_cache,
@@ -165,7 +178,8 @@ pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const void *v_c
     if (num_partitions < 0) return PA_ERR_INVALID_ARG;
     return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
                        scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       num_blocks, workspace, workspace_bytes, num_partitions, stream);
+                       num_blocks, PA_LAYOUT_TOKEN_MAJOR, workspace, workspace_bytes,
+                       num_partitions, stream);
 }
 
 size_t pa_decode_multi_workspace_size(int q_len, int num_q_heads, int num_kv_heads,
@@ -179,6 +193,18 @@ size_t pa_decode_multi_workspace_size(int q_len, int num_q_heads, int num_kv_hea
     return P > 0 ? pa::decode_workspace_bytes(gp, P) : 0;
 }
 
+pa_status_t pa_decode_layout(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, float scale, void *out, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks, pa_layout_t layout, void *workspace,
+                             size_t workspace_bytes, int num_partitions, void *stream) {
+    if (num_partitions < 0) return PA_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
+                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, layout, workspace, workspace_bytes, num_partitions, stream);
+}
+
 pa_status_t pa_decode_multi(const void *q, const void *k_cache, const void *v_cache,
                             const int32_t *block_tables, int max_blocks_per_seq,
                             const int32_t *context_lens, int q_len, float scale, void *out,
@@ -187,7 +213,8 @@ pa_status_t pa_decode_multi(const void *q, const void *k_cache, const void *v_ca
                             size_t workspace_bytes, void *stream) {
     return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        q_len, scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                       block_size, num_blocks, workspace, workspace_bytes, 0, stream);
+                       block_size, num_blocks, PA_LAYOUT_TOKEN_MAJOR, workspace,
+                       workspace_bytes, 0, stream);
 }
 
 }  // extern "C"

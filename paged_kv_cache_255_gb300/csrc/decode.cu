@@ -97,8 +97,12 @@ __device__ __forceinline__ void issue_tile(const Cursor &c, int bid, uint8_t *st
     int valid = tile_valid(c);
     if (bid < 0 || (int64_t)bid >= a.num_blocks) valid = 0;   // never address outside the pool
     const int off = (c.j << 4) & ((1 << a.block_size_log2) - 1);
-    const int64_t row0 = ((((int64_t)bid << a.block_size_log2) + off) * a.num_kv_heads + c.kvh);
-    const int64_t rstride = (int64_t)a.num_kv_heads * kRowBytes;
+    // token-major pool [NB][bs][Hkv][D]: a tile's rows are Hkv rows apart;
+    // head-major pool [NB][Hkv][bs][D]: they are one contiguous run
+    const int64_t row0 = a.head_major
+        ? ((((int64_t)bid * a.num_kv_heads + c.kvh) << a.block_size_log2) + off)
+        : ((((int64_t)bid << a.block_size_log2) + off) * a.num_kv_heads + c.kvh);
+    const int64_t rstride = a.head_major ? (int64_t)kRowBytes : (int64_t)a.num_kv_heads * kRowBytes;
     const char *kb = static_cast<const char *>(a.k_cache) + row0 * kRowBytes;
     const char *vb = static_cast<const char *>(a.v_cache) + row0 * kRowBytes;
     const int chunk = lane & 15;

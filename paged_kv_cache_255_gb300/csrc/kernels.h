@@ -31,6 +31,7 @@ struct DecodeArgs {
     int q_len;                  // query tokens per sequence (1: plain decode)
     int cols;                   // q_len * group: (query token, head) columns per KV head
     int block_size_log2;
+    int head_major;             // pool layout: 0 [NB, bs, Hkv, D], 1 [NB, Hkv, bs, D]
     int max_blocks_per_seq;
     int64_t num_blocks;
     float scale_log2;           // scale * log2(e)
@@ -54,7 +55,9 @@ void decode_carve_workspace(DecodeArgs &a, void *workspace, int group_pad);
 cudaError_t launch_decode(const DecodeArgs &a, int group_pad, DecodeKernel k, cudaStream_t stream);
 
 cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
-                                 const int64_t *slot_mapping, int64_t num_tokens, int row_elems,
-                                 int64_t num_slots, int sm_count, cudaStream_t stream);
+                                 const int64_t *slot_mapping, int64_t num_tokens,
+                                 int num_kv_heads, int head_dim, int block_size_log2,
+                                 int64_t num_slots, int head_major, int sm_count,
+                                 cudaStream_t stream);
 
 }  // namespace pa

@@ -15,15 +15,17 @@ namespace {
 
 constexpr int kStoreWarps = 8;
 
+template <bool HEAD_MAJOR>
 __global__ void __launch_bounds__(kStoreWarps * 32)
 store_kvcache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
                      uint4 *__restrict__ k_cache, uint4 *__restrict__ v_cache,
                      const int64_t *__restrict__ slot_mapping, int64_t num_tokens,
-                     int row_chunks, int64_t num_slots) {
+                     int num_kv_heads, int head_chunks, int block_size_log2, int64_t num_slots) {
     // let a decode launched as a programmatic dependent start its launch now;
     // it still waits for this grid to finish before reading the cache
     asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
     const int lane = threadIdx.x & 31;
+    const int row_chunks = num_kv_heads * head_chunks;     // 16-byte chunks per row
     const int64_t first = (int64_t)blockIdx.x * kStoreWarps + (threadIdx.x >> 5);
     const int64_t stride = (int64_t)gridDim.x * kStoreWarps;
     for (int64_t i = first; i < num_tokens; i += stride) {
@@ -31,13 +33,21 @@ store_kvcache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
         if (slot < 0 || slot >= num_slots) continue;   // -1 padding, or out of range
         const uint4 *ks = k + i * row_chunks;
         const uint4 *vs = v + i * row_chunks;
-        uint4 *kd = k_cache + slot * row_chunks;
-        uint4 *vd = v_cache + slot * row_chunks;
         for (int c = lane; c < row_chunks; c += 32) {
+            // token-major: the row is contiguous at the slot; head-major: head
+            // h's part goes to row (block, h, off) of the [NB][Hkv][bs][D] pool
+            int64_t dst = slot * row_chunks + c;
+            if (HEAD_MAJOR) {
+                const int64_t block = slot >> block_size_log2;
+                const int64_t off = slot & ((1 << block_size_log2) - 1);
+                const int h = c / head_chunks;
+                dst = (((block * num_kv_heads + h) << block_size_log2) + off) * head_chunks +
+                      (c - h * head_chunks);
+            }
             const uint4 a = __ldg(ks + c);
             const uint4 b = __ldg(vs + c);
-            kd[c] = a;
-            vd[c] = b;
+            k_cache[dst] = a;
+            v_cache[dst] = b;
         }
     }
 }
@@ -46,17 +56,18 @@ store_kvcache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
 
 cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
                                  const int64_t *slot_mapping, int64_t num_tokens,
-                                 int row_elems, int64_t num_slots, int sm_count,
+                                 int num_kv_heads, int head_dim, int block_size_log2,
+                                 int64_t num_slots, int head_major, int sm_count,
                                  cudaStream_t stream) {
     if (num_tokens == 0) return cudaSuccess;
-    const int row_chunks = row_elems / 8;   // 16-byte chunks per row
     int64_t blocks = (num_tokens + kStoreWarps - 1) / kStoreWarps;
     const int64_t cap = (int64_t)sm_count * 16;
     if (blocks > cap) blocks = cap;
-    store_kvcache_kernel<<<(unsigned)blocks, kStoreWarps * 32, 0, stream>>>(
+    auto kernel = head_major ? store_kvcache_kernel<true> : store_kvcache_kernel<false>;
+    kernel<<<(unsigned)blocks, kStoreWarps * 32, 0, stream>>>(
         static_cast<const uint4 *>(k), static_cast<const uint4 *>(v),
         static_cast<uint4 *>(k_cache), static_cast<uint4 *>(v_cache), slot_mapping, num_tokens,
-        row_chunks, num_slots);
+        num_kv_heads, head_dim / 8, block_size_log2, num_slots);
     return cudaGetLastError();
 }
 

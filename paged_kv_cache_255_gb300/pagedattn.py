@@ -32,6 +32,10 @@ SIGNATURES = {
     "pa_decode_noalloc": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                            _I64, _P], _I32),
     "pa_decode_multi_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
+    "pa_store_kvcache_layout": ([_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64, _I32, _P],
+                                _I32),
+    "pa_decode_layout": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32, _I64,
+                          _I32, _P, _SZ, _I32, _P], _I32),
     "pa_decode_multi": ([_P, _P, _P, _P, _I32, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                          _I64, _P, _SZ, _P], _I32),
 }
@@ -96,25 +100,30 @@ def _cuda(t: torch.Tensor, name: str, dtype, device=None):
         raise ValueError(f"{name} is on {t.device}, expected {device}")
 
 
-def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None):
+def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None, head_major=False):
     """Write row i of k/v to cache slot slot_mapping[i] (-1 rows skipped).
 
-    k, v: bf16 [N, Hkv, D]; k_cache, v_cache: bf16 [NB, bs, Hkv, D];
-    slot_mapping: int64 [N]. Runs on the current stream (or ``stream``).
+    k, v: bf16 [N, Hkv, D]; k_cache, v_cache: bf16 [NB, bs, Hkv, D], or
+    [NB, Hkv, bs, D] with ``head_major``; slot_mapping: int64 [N]. Runs on the
+    current stream (or ``stream``).
     """
     dev = k_cache.device
     for t, n, dt in ((k, "k", torch.bfloat16), (v, "v", torch.bfloat16),
                      (k_cache, "k_cache", torch.bfloat16), (v_cache, "v_cache", torch.bfloat16),
                      (slot_mapping, "slot_mapping", torch.int64)):
         _cuda(t, n, dt, dev)
-    NB, bs, Hkv, D = k_cache.shape
+    if head_major:
+        NB, Hkv, bs, D = k_cache.shape
+    else:
+        NB, bs, Hkv, D = k_cache.shape
     N = slot_mapping.shape[0]
     if v_cache.shape != k_cache.shape or k.shape != (N, Hkv, D) or v.shape != (N, Hkv, D):
         raise ValueError("shape mismatch between k, v, caches and slot_mapping")
     with torch.cuda.device(dev):
-        st = lib().pa_store_kvcache(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(),
-                                    v_cache.data_ptr(), slot_mapping.data_ptr(), N, Hkv, D, bs,
-                                    NB, _stream_ptr(stream, dev))
+        st = lib().pa_store_kvcache_layout(k.data_ptr(), v.data_ptr(), k_cache.data_ptr(),
+                                           v_cache.data_ptr(), slot_mapping.data_ptr(), N, Hkv,
+                                           D, bs, NB, 1 if head_major else 0,
+                                           _stream_ptr(stream, dev))
     _check("pa_store_kvcache", st)
 
 
@@ -141,12 +150,13 @@ def workspace_for(num_q_heads, num_kv_heads, head_dim=128, num_partitions=0, dev
 
 
 def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, workspace=None,
-           num_partitions: int = 0, stream=None):
+           num_partitions: int = 0, stream=None, head_major=False):
     """Single-token paged decode attention; returns ``out`` (bf16 [S, Hq, D]).
 
-    q: bf16 [S, Hq, D]; caches: bf16 [NB, bs, Hkv, D]; block_tables: int32
-    [S, max_blocks]; context_lens: int32 [S]. ``num_partitions`` > 0 forces
-    the split-K share count (pa_decode_splitk).
+    q: bf16 [S, Hq, D]; caches: bf16 [NB, bs, Hkv, D] ([NB, Hkv, bs, D] with
+    ``head_major``); block_tables: int32 [S, max_blocks]; context_lens: int32
+    [S]. ``num_partitions`` > 0 forces the split-K share count
+    (pa_decode_splitk).
     """
     dev = q.device
     for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
@@ -154,7 +164,10 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
                      (context_lens, "context_lens", torch.int32)):
         _cuda(t, n, dt, dev)
     S, Hq, D = q.shape
-    NB, bs, Hkv, D2 = k_cache.shape
+    if head_major:
+        NB, Hkv, bs, D2 = k_cache.shape
+    else:
+        NB, bs, Hkv, D2 = k_cache.shape
     if v_cache.shape != k_cache.shape or D2 != D or block_tables.dim() != 2 \
             or block_tables.shape[0] != S or context_lens.shape != (S,):
         raise ValueError("shape mismatch between q, caches, block_tables and context_lens")
@@ -173,7 +186,10 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
             block_tables.shape[1], context_lens.data_ptr(), float(scale), out.data_ptr(), S, Hq,
             Hkv, D, bs, NB, workspace.data_ptr(), ws_bytes)
     with torch.cuda.device(dev):
-        if num_partitions:
+        if head_major:
+            st = lib().pa_decode_layout(*args[:14], 1, *args[14:], int(num_partitions),
+                                        _stream_ptr(stream, dev))
+        elif num_partitions:
             st = lib().pa_decode_splitk(*args, int(num_partitions), _stream_ptr(stream, dev))
         else:
             st = lib().pa_decode(*args, _stream_ptr(stream, dev))
@@ -242,10 +258,10 @@ class DecodeStepGraph:
 
     def __init__(self, q, k_cache, v_cache, block_tables, context_lens, scale, k_new=None,
                  v_new=None, slot_mapping=None, out=None, host_stage=None, device_stage=None,
-                 host_out=None):
+                 host_out=None, head_major=False):
         dev = q.device
         S, Hq, D = q.shape
-        Hkv = k_cache.shape[2]
+        Hkv = k_cache.shape[1] if head_major else k_cache.shape[2]
         self.out = out if out is not None else torch.empty_like(q)
         self.workspace = workspace_for(Hq, Hkv, D, 0, dev)
         has_store = slot_mapping is not None and slot_mapping.shape[0] > 0
@@ -254,9 +270,9 @@ class DecodeStepGraph:
             if host_stage is not None:
                 device_stage.copy_(host_stage, non_blocking=True)
             if has_store:
-                store_kvcache(k_new, v_new, k_cache, v_cache, slot_mapping)
+                store_kvcache(k_new, v_new, k_cache, v_cache, slot_mapping, head_major=head_major)
             decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=self.out,
-                   workspace=self.workspace)
+                   workspace=self.workspace, head_major=head_major)
             if host_out is not None:
                 host_out.copy_(self.out, non_blocking=True)
 
