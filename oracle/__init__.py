@@ -90,6 +90,9 @@ class Oracle:
         lib.oracle_decode_layout.argtypes = [p, p, p, p, i32, p, dbl, p, i32, i32, i32, i32, i32,
                                              i64, i32, i32]
         lib.oracle_decode_layout.restype = i32
+        lib.oracle_prefill.argtypes = [p, p, p, p, i32, p, p, dbl, p, i32, i32, i32, i32, i32,
+                                       i32, i64, i32]
+        lib.oracle_prefill.restype = i32
         lib.oracle_num_threads.argtypes = []
         lib.oracle_num_threads.restype = i32
         self.lib = lib
@@ -193,6 +196,25 @@ class Oracle:
             raise OracleError(f"oracle_decode_layout returned {rc}")
         return out
 
+    def prefill(self, q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale,
+                threads: int = 0):
+        """fp64 [total_q, Hq, D] prefill outputs; rows of q ([total_q, Hq, D]) are
+        packed per sequence by query_start_loc ([S + 1])."""
+        qb, kc, vc = _bits(q), _bits(k_cache), _bits(v_cache)
+        bt = _arr(block_tables, np.int32)
+        cl = _arr(context_lens, np.int32)
+        qsl = _arr(query_start_loc, np.int32)
+        T, Hq, D = qb.shape
+        NB, bs, Hkv, _ = kc.shape
+        S = cl.shape[0]
+        out = np.zeros((T, Hq, D), dtype=np.float64)
+        rc = self.lib.oracle_prefill(_ptr(qb), _ptr(kc), _ptr(vc), _ptr(bt), bt.shape[1],
+                                     _ptr(cl), _ptr(qsl), float(scale), _ptr(out), S, T, Hq, Hkv,
+                                     D, bs, NB, int(threads))
+        if rc != OK:
+            raise OracleError(f"oracle_prefill returned {rc}")
+        return out
+
     def decode_multi(self, q, k_cache, v_cache, block_tables, context_lens, scale,
                      threads: int = 0):
         """fp64 [S, Q, Hq, D] outputs for Q new tokens per sequence (q is
@@ -247,3 +269,7 @@ def decode_pairs(*a, **kw):
 
 def decode_multi(*a, **kw):
     return get().decode_multi(*a, **kw)
+
+
+def prefill(*a, **kw):
+    return get().prefill(*a, **kw)

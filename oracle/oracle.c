@@ -310,6 +310,61 @@ int oracle_decode_multi(const uint16_t *q, const uint16_t *k_cache, const uint16
     return err;
 }
 
+/*
+ * Prefill of a chunk of new tokens per sequence over the paged cache (the
+ * prompt phase, "A vLLM engine small enough to read in one sitting": prefill
+ * and decode both run over the paged KV cache). The rows of q are packed
+ * sequence after sequence: sequence s owns rows [query_start_loc[s],
+ * query_start_loc[s + 1]); with n_s of them, row i of the sequence is the
+ * token at position context_lens[s] - n_s + i and attends causally to tokens
+ * t <= context_lens[s] - n_s + i (all of them stored in the cache). q and out
+ * are [total_q, num_q_heads, head_dim].
+ */
+int oracle_prefill(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                   const int32_t *block_tables, int max_blocks_per_seq,
+                   const int32_t *context_lens, const int32_t *query_start_loc, double scale,
+                   double *out, int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
+                   int head_dim, int block_size, int64_t num_blocks, int num_threads)
+{
+    int rc = check_shape(num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                         max_blocks_per_seq);
+    if (rc != ORACLE_OK)
+        return rc;
+    if (total_q < 0 || query_start_loc[0] != 0 || query_start_loc[num_seqs] != total_q)
+        return ORACLE_ERR_ARG;
+    for (int s = 0; s < num_seqs; ++s)
+        if (query_start_loc[s + 1] < query_start_loc[s])
+            return ORACLE_ERR_ARG;
+    const int64_t total = (int64_t)total_q * num_q_heads;
+    int err = ORACLE_OK;
+#ifdef _OPENMP
+    if (num_threads <= 0)
+        num_threads = omp_get_max_threads();
+#pragma omp parallel for schedule(dynamic, 16) num_threads(num_threads)
+#endif
+    for (int64_t r_i = 0; r_i < total; ++r_i) {
+        const int row = (int)(r_i / num_q_heads);
+        int s = 0;
+        while (query_start_loc[s + 1] <= row)
+            ++s;
+        const int n = query_start_loc[s + 1] - query_start_loc[s];
+        const int i = row - query_start_loc[s];
+        const int cap = context_lens[s] - n + i + 1;
+        int r = decode_one(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                           scale, s, (int)(r_i % num_q_heads), num_q_heads, num_kv_heads,
+                           head_dim, block_size, num_blocks, row, cap,
+                           ORACLE_LAYOUT_TOKEN_MAJOR, out + r_i * head_dim);
+        if (r != ORACLE_OK) {
+#ifdef _OPENMP
+#pragma omp critical
+#endif
+            err = r;
+        }
+    }
+    (void)num_threads;
+    return err;
+}
+
 int oracle_num_threads(void)
 {
 #ifdef _OPENMP

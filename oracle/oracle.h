@@ -75,6 +75,16 @@ int oracle_decode_layout(const uint16_t *q, const uint16_t *k_cache, const uint1
                          int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                          int block_size, int64_t num_blocks, int layout, int num_threads);
 
+/* Prefill: rows [query_start_loc[s], query_start_loc[s + 1]) of q belong to
+ * sequence s; with n_s of them, row i is the token at position
+ * context_lens[s] - n_s + i and attends to tokens t <= that position.
+ * q and out are [total_q, num_q_heads, head_dim]. */
+int oracle_prefill(const uint16_t *q, const uint16_t *k_cache, const uint16_t *v_cache,
+                   const int32_t *block_tables, int max_blocks_per_seq,
+                   const int32_t *context_lens, const int32_t *query_start_loc, double scale,
+                   double *out, int num_seqs, int total_q, int num_q_heads, int num_kv_heads,
+                   int head_dim, int block_size, int64_t num_blocks, int num_threads);
+
 /* Threads the OpenMP loops use by default. */
 int oracle_num_threads(void);
 

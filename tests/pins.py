@@ -346,6 +346,47 @@ def pin_head_major(O):
         assert np.array_equal(a, b), "head-major decode"
 
 
+def _prefill_case(seed, lens, chunks, Hq=8, Hkv=2, bs=16):
+    """A pool holding len(lens) sequences and a packed query block of
+    chunks[s] <= lens[s] new tokens per sequence."""
+    spec = inputs.Spec("pf", ((len(lens), 1, 1),), Hq, Hkv, bs, store_mode="none")
+    wl = inputs.generate(spec, seed=seed, keep_content=True, context_lens=lens)
+    qsl = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    g = torch.Generator().manual_seed(seed)
+    q = torch.randn((int(qsl[-1]), Hq, 128), generator=g).to(BF16)
+    return wl, q, qsl
+
+
+def pin_prefill_sdpa(O):
+    """Prefill rows against torch's fp64 SDPA with an explicit causal mask."""
+    lens, chunks = [37, 200, 16, 129, 5], [37, 64, 1, 100, 5]
+    wl, q, qsl = _prefill_case(71, lens, chunks)
+    out = O.prefill(q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, qsl, wl.scale)
+    for s in range(len(lens)):
+        L, n = lens[s], chunks[s]
+        k, v = wl.logical_kv(s, after_store=False)
+        qq = q[qsl[s]:qsl[s + 1]].double().permute(1, 0, 2)[None]      # [1, Hq, n, D]
+        kk = k.double().permute(1, 0, 2)[None]
+        vv = v.double().permute(1, 0, 2)[None]
+        mask = torch.arange(L)[None, :] <= (L - n + torch.arange(n))[:, None]
+        ref = F.scaled_dot_product_attention(qq, kk, vv, attn_mask=mask, scale=wl.scale,
+                                             enable_gqa=True)[0].permute(1, 0, 2).numpy()
+        err = np.abs(out[qsl[s]:qsl[s + 1]] - ref).max()
+        assert err <= 1e-10, f"prefill seq {s}: max err {err}"
+
+
+def pin_prefill_is_multi_token(O):
+    """With the same number Q of new tokens in every sequence, prefill is the
+    multi-token decode of the same rows."""
+    lens, Q = [40, 90, 17, 33], 4
+    wl, q, qsl = _prefill_case(72, lens, [Q] * len(lens))
+    a = O.prefill(q, wl.k_cache, wl.v_cache, wl.block_tables, wl.context_lens, qsl, wl.scale)
+    b = O.decode_multi(q.view(len(lens), Q, *q.shape[1:]), wl.k_cache, wl.v_cache,
+                       wl.block_tables, wl.context_lens, wl.scale)
+    assert np.array_equal(a, b.reshape(a.shape))
+
+
 ALL_PINS = [pin_sdpa, pin_single_token, pin_zero_keys, pin_unit_values, pin_three_tokens,
             pin_dominant_key, pin_renumbering, pin_prefix_private, pin_block_size,
-            pin_nan_free, pin_store, pin_multi_sdpa, pin_multi_prefix, pin_head_major]
+            pin_nan_free, pin_store, pin_multi_sdpa, pin_multi_prefix, pin_head_major,
+            pin_prefill_sdpa, pin_prefill_is_multi_token]

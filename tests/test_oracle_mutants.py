@@ -33,6 +33,8 @@ MUTANTS = [
      "? k_cache + ((block * block_size + t % block_size) * num_kv_heads + kvh) * (int64_t)head_dim"),
     ("head_major_store_head_stride", "const int64_t dst = ((block * num_kv_heads + h) * block_size + off) * head_dim;",
      "const int64_t dst = ((block * block_size + off) * num_kv_heads + h) * head_dim;"),
+    ("prefill_row_offset", "const int cap = context_lens[s] - n + i + 1;",
+     "const int cap = context_lens[s] - n + i;"),
     ("store_skips_first_row", "if (slot == -1)\n            continue;",
      "if (slot == -1 || i == 0)\n            continue;"),
 ]
