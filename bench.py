@@ -39,6 +39,8 @@ METRIC = "paged-decode µs/step and KV-read GB/s (fraction of GB300 HBM peak)"
 DEFAULT_WORKLOAD = "qwen3_0_6b"
 L2_FLUSH_BYTES = 512 << 20       # > 2x the 129 MB L2
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+PREFILL_METRIC = "paged-prefill µs/step and attention TFLOP/s (fraction of GB300 bf16 tensor peak)"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 KERNEL_SOURCES = ["paged_kv_cache_255_gb300/csrc/decode.cu", "paged_kv_cache_255_gb300/csrc/common.cuh"]
 
@@ -51,14 +53,14 @@ def kernel_hash() -> str:
     return h.hexdigest()[:16]
 
 
-def measured_peaks():
+def measured_peaks(key="hbm_gbs"):
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
         with open(path) as f:
             d = json.load(f)
-        return float(d["hbm_gbs"]), "measured"
+        return float(d[key]), "measured"
     except Exception:
-        return FALLBACK_HBM_GBS, "fallback"
+        return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}[key], "fallback"
 
 
 def ncu_traffic(workload: str):
@@ -433,12 +435,202 @@ def run_gpu(args, rank, world, local):
     print(json.dumps(line), flush=True)
 
 
+def prefill_flops(pb) -> int:
+    """Algorithmic FLOPs of one prefill launch: per causal (row, key) pair and
+    query head, a 128-long dot product for the score and a 128-long
+    multiply-add of V, 2 * 128 FLOPs each."""
+    return 4 * pb.wl.spec.head_dim * pb.wl.spec.num_q_heads * pb.causal_pairs()
+
+
+def prefill_config(pb, chunk):
+    c = workload_config(pb.wl)
+    c.update(store_rows=int(pb.slot_mapping.shape[0]), query_rows=int(pb.query_start_loc[-1]),
+             max_query_len=pb.max_query_len, chunk="whole prompt" if chunk is None else chunk,
+             causal_pairs=pb.causal_pairs())
+    return c
+
+
+def prefill_oracle_sample(pb, target_s: float, host=None):
+    """Time the fp64 oracle on random rows of the prefill step (each row as a
+    one-row chunk of its sequence cut at its causal limit) and scale by causal
+    (row, key) pairs to the whole step, plus the oracle store of all chunk rows.
+    Returns (us_per_step, threads, sample description)."""
+    import oracle
+    O = oracle.get()
+    threads = O.num_threads()
+    if host is None:
+        host = (pb.wl.k_cache, pb.wl.v_cache)
+    kc, vc = oracle._bits(host[0]).copy(), oracle._bits(host[1]).copy()
+    t0 = time.perf_counter()
+    O.store_kvcache_into(pb.k_new, pb.v_new, kc, vc, pb.slot_mapping)
+    t_store = time.perf_counter() - t0
+    qsl = pb.query_start_loc
+    T = int(qsl[-1])
+    seq_of = np.searchsorted(qsl, np.arange(T), side="right") - 1
+    n = np.diff(qsl)[seq_of]
+    cut = (pb.wl.context_lens[seq_of].astype(np.int64) - n + (np.arange(T) - qsl[seq_of]) + 1)
+    rng = np.random.Generator(np.random.PCG64(321))
+    order = rng.permutation(T)
+    done, done_pairs, elapsed, batch = 0, 0, 0.0, max(threads, 4)
+    while elapsed < target_s:
+        idx = order[done % T:done % T + batch]
+        t0 = time.perf_counter()
+        O.prefill(pb.q[torch.from_numpy(idx)], kc, vc, pb.wl.block_tables[seq_of[idx]],
+                  cut[idx].astype(np.int32), np.arange(len(idx) + 1, dtype=np.int32),
+                  pb.wl.scale)
+        elapsed += time.perf_counter() - t0
+        done += len(idx)
+        done_pairs += int(cut[idx].sum())
+        batch = min(batch * 2, 1024)
+    us = (t_store + elapsed * pb.causal_pairs() / max(done_pairs, 1)) * 1e6
+    sample = (f"oracle store of all {T} chunk rows + {done} random query rows (all "
+              f"{pb.wl.spec.num_q_heads} heads) out of {T} ({elapsed:.1f} s of oracle time), "
+              f"scaled by causal (row, key) pairs to one full step")
+    return us, threads, sample
+
+
+def run_reference_prefill(args, rank, world):
+    if rank != 0:
+        return
+    spec, chunk = inputs.PREFILL_SPECS[args.workload]
+    pb = inputs.prefill_batch(spec, seed=0, chunk=chunk)
+    per_step = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
+    for _ in range(args.warmup):
+        prefill_oracle_sample(pb, per_step)
+    vals = []
+    for _ in range(args.steps):
+        us, threads, sample = prefill_oracle_sample(pb, per_step)
+        vals.append(us)
+    v = statistics.median(vals)
+    line = {"impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "us/step",
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3,
+            "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "config": prefill_config(pb, chunk),
+            "cpu_baseline": {"value": v, "unit": "us/step", "cores": threads, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": v, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_gpu_prefill(args, rank, world, local):
+    """One prefill step: store of every chunk row's K/V, then paged prefill."""
+    from paged_kv_cache_255_gb300 import pagedattn as pa
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    spec, chunk = inputs.PREFILL_SPECS[args.workload]
+    pb = inputs.prefill_batch(spec, seed=0, chunk=chunk)
+    wl = pb.wl
+    k_cache, v_cache = wl.k_cache.to(dev), wl.v_cache.to(dev)
+    host_inputs = [pb.q, pb.k_new, pb.v_new, torch.from_numpy(pb.slot_mapping),
+                   torch.from_numpy(wl.block_tables), torch.from_numpy(wl.context_lens),
+                   torch.from_numpy(pb.query_start_loc)]
+    q, k_new, v_new, slots, bt, cl, qsl = [t.to(dev) for t in host_inputs]
+    out = torch.empty_like(q)
+    mql = pb.max_query_len
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step(q_, kn_, vn_, sl_, bt_, cl_, qsl_):
+        pa.store_kvcache(kn_, vn_, k_cache, v_cache, sl_)
+        pa.prefill(q_, k_cache, v_cache, bt_, cl_, qsl_, wl.scale, max_query_len=mql, out=out)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        step(q, k_new, v_new, slots, bt, cl, qsl)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots)
+        ev[i][1].record(stream)
+        pa.prefill(q, k_cache, v_cache, bt, cl, qsl, wl.scale, max_query_len=mql, out=out)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    clk = clocks.stop()
+    step_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in ev), world)
+    store_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev), world)
+    pf_ms = max_over_ranks(statistics.mean(e[1].elapsed_time(e[2]) for e in ev), world)
+
+    # end to end: pinned host inputs packed in one staging buffer, one H2D,
+    # the step, the output read back
+    offs, total = [], 0
+    for t in host_inputs:
+        offs.append(total)
+        total += (t.numel() * t.element_size() + 255) // 256 * 256
+    h_stage = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    for t, o in zip(host_inputs, offs):
+        nb = t.numel() * t.element_size()
+        h_stage[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+    d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
+    views = [d_stage[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+             for t, o in zip(host_inputs, offs)]
+    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
+    d2h = hout.numel() * hout.element_size()
+
+    def e2e_step():
+        d_stage.copy_(h_stage, non_blocking=True)
+        step(*views)
+        hout.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a_.record(stream)
+        e2e_step()
+        b_.record(stream)
+        b_.synchronize()
+        e2e_ms.append(a_.elapsed_time(b_))
+    e2e = max_over_ranks(statistics.mean(e2e_ms), world)
+    torch.cuda.synchronize()
+    if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
+        raise SystemExit("e2e output differs from the device-resident output")
+    if rank != 0:
+        return
+    flops = prefill_flops(pb)
+    peak, peak_src = measured_peaks("bf16_tflops")
+    achieved = flops / (pf_ms * 1e-3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": step_ms * 1e3, "unit": "us/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic", "config": prefill_config(pb, chunk),
+        "store_us": store_ms * 1e3, "prefill_us": pf_ms * 1e3,
+        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                     "frac": achieved / peak, "traffic": None, "kernel": "pa_prefill",
+                     "algorithmic_flops": flops,
+                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "e2e": {"value": e2e * 1e3, "unit": "us/step", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": args.steps * 2,
+        "timing": "value: store + prefill per step, events between the two calls",
+        "clocks": clk,
+    }
+    if not args.no_cpu_baseline:
+        us, threads, sample = prefill_oracle_sample(pb, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": us, "unit": "us/step", "cores": threads,
+                                "kind": "oracle", "sample": sample}
+    print(json.dumps(line), flush=True)
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(inputs.SPECS))
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=sorted(inputs.SPECS) + sorted(inputs.PREFILL_SPECS),
+                    help="a decode step, or a prefill step (%s)" % ", ".join(inputs.PREFILL_SPECS))
     ap.add_argument("--num-seqs", type=int, default=0,
                     help="run a copy of the workload with this many sequences (profiling)")
     ap.add_argument("--q-len", type=int, default=1,
@@ -453,12 +645,13 @@ def main():
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
     rank, world, local = dist_setup(args.gpus)
+    prefill = args.workload in inputs.PREFILL_SPECS
     if args.impl == "reference":
-        run_reference(args, rank, world)
+        (run_reference_prefill if prefill else run_reference)(args, rank, world)
     else:
         if not torch.cuda.is_available():
             raise SystemExit("bench.py needs a CUDA device")
-        run_gpu(args, rank, world, local)
+        (run_gpu_prefill if prefill else run_gpu)(args, rank, world, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

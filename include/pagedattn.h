@@ -235,6 +235,32 @@ PA_API pa_status_t pa_decode_layout(const void *q, const void *k_cache, const vo
                                     pa_layout_t layout, void *workspace, size_t workspace_bytes,
                                     int num_partitions, void *stream);
 
+/*
+ * Paged prefill (chunked prefill): a chunk of new tokens per sequence attends
+ * causally to the sequence's tokens in the paged cache, as in the engine's
+ * prefill phase ("A vLLM engine small enough to read in one sitting": prefill
+ * and decode over the paged KV cache, flash attention for prefill).
+ *
+ * q and out are [total_q, num_q_heads, head_dim] bf16, rows packed sequence
+ * after sequence: sequence s owns rows [query_start_loc[s],
+ * query_start_loc[s + 1]) (query_start_loc: int32 [num_seqs + 1] on the device,
+ * starting at 0 and non-decreasing). With n_s rows and L = context_lens[s]
+ * counting them (their K/V already stored, e.g. by pa_store_kvcache), row i of
+ * sequence s is the token at position L - n_s + i and, for query head h,
+ *   out = sum_{t <= L - n_s + i} softmax_t(scale * q . K_t) V_t
+ * with K_t, V_t of KV head h / (num_q_heads / num_kv_heads) gathered through the
+ * block table. A row with no visible token outputs zero. max_query_len is a
+ * host-side hint for the grid (the largest n_s; a smaller value is still
+ * correct, only slower). Token-major pool layout; group size <= 16; head_dim
+ * 128. Computes in fp32 on the tensor cores, output bf16. Allocates nothing.
+ */
+PA_API pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, const int32_t *query_start_loc,
+                              int max_query_len, float scale, void *out, int num_seqs,
+                              int total_q, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int64_t num_blocks, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -217,4 +217,47 @@ pa_status_t pa_decode_multi(const void *q, const void *k_cache, const void *v_ca
                        workspace_bytes, 0, stream);
 }
 
+pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *context_lens, const int32_t *query_start_loc,
+                       int max_query_len, float scale, void *out, int num_seqs, int total_q,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int64_t num_blocks, void *stream) {
+    if (num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_blocks < 0 || max_blocks_per_seq < 0 || max_query_len < 0 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (head_dim != pa::kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+    const int group = num_q_heads / num_kv_heads;
+    const int gp = pa::decode_group_pad(group);
+    if (gp == 0) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0 || total_q == 0) return PA_OK;
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !query_start_loc || !out)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_INVALID_ARG;
+    if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    pa::PrefillArgs a{};
+    a.q = q;
+    a.k_cache = k_cache;
+    a.v_cache = v_cache;
+    a.block_tables = block_tables;
+    a.context_lens = context_lens;
+    a.query_start_loc = query_start_loc;
+    a.out = out;
+    a.num_seqs = num_seqs;
+    a.total_q = total_q;
+    a.num_q_heads = num_q_heads;
+    a.num_kv_heads = num_kv_heads;
+    a.group = group;
+    a.block_size_log2 = log2_exact(block_size);
+    a.max_blocks_per_seq = max_blocks_per_seq;
+    a.num_blocks = num_blocks;
+    a.scale_log2 = (float)((double)scale * 1.4426950408889634);
+    const cudaError_t e = pa::launch_prefill(a, gp, max_query_len > 0 ? max_query_len : 1,
+                                             static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
 }  // extern "C"

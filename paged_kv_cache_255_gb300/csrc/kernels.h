@@ -54,6 +54,29 @@ void decode_carve_workspace(DecodeArgs &a, void *workspace, int group_pad);
 
 cudaError_t launch_decode(const DecodeArgs &a, int group_pad, DecodeKernel k, cudaStream_t stream);
 
+// One paged-prefill launch (pointers are device memory).
+struct PrefillArgs {
+    const void *q;                  // bf16 [total_q, Hq, 128], rows packed per sequence
+    const void *k_cache;            // bf16 [NB, bs, Hkv, 128]
+    const void *v_cache;
+    const int32_t *block_tables;    // [S, max_blocks_per_seq]
+    const int32_t *context_lens;    // [S], counting each sequence's new tokens
+    const int32_t *query_start_loc; // [S + 1]
+    void *out;                      // bf16 [total_q, Hq, 128]
+    int num_seqs;
+    int total_q;
+    int num_q_heads;
+    int num_kv_heads;
+    int group;
+    int block_size_log2;
+    int max_blocks_per_seq;
+    int64_t num_blocks;
+    float scale_log2;
+};
+
+cudaError_t launch_prefill(const PrefillArgs &a, int group_pad, int max_query_len,
+                           cudaStream_t stream);
+
 cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
                                  const int64_t *slot_mapping, int64_t num_tokens,
                                  int num_kv_heads, int head_dim, int block_size_log2,

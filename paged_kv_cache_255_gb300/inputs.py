@@ -348,3 +348,87 @@ def generate(spec: Spec, seed: int = 0, device="cpu", keep_content: bool = False
         wl.content_k = ck.cpu()
         wl.content_v = cv.cpu()
     return wl
+
+
+# -- prefill batches ---------------------------------------------------------
+#
+# A prefill step takes a chunk of n_s new tokens per sequence (n_s <= L_s, the
+# last n_s positions of the sequence): their K/V rows are stored through a
+# slot mapping, then every chunk row attends causally to the sequence's first
+# L_s - n_s + i + 1 tokens. The pool holds the earlier L_s - n_s tokens; the
+# rows the store is about to write hold NaN until it does.
+
+# name -> (pool spec, chunk): chunk None means the whole prompt (n_s = L_s),
+# an int c means n_s = min(c, L_s).
+PREFILL_SPECS = {
+    # 60 batched prompts of 64..1024 tokens, Qwen3-0.6B attention shape
+    # (16 q / 8 KV heads): the prompt phase of the 60-prompt decode batch.
+    "qwen3_0_6b_prompts": (Spec("qwen3_0_6b_prompts", ((60, 64, 1024),), 16, 8, 16,
+                                pool_factor=1.2, store_mode="none"), None),
+    # chunked prefill: 32 sequences with 2k..8k tokens of context each take a
+    # 512-token chunk, Qwen3-8B attention shape (32 q / 8 KV heads).
+    "chunked_8b": (Spec("chunked_8b", ((32, 2048, 8192),), 32, 8, 16,
+                        store_mode="none"), 512),
+}
+
+
+@dataclasses.dataclass
+class PrefillBatch:
+    wl: Workload                  # pool, tables and lengths (L_s counts the chunk)
+    query_start_loc: np.ndarray   # int32 [S + 1]
+    q: torch.Tensor               # bf16 [T, Hq, D]
+    k_new: torch.Tensor           # bf16 [T, Hkv, D], the chunk rows' K
+    v_new: torch.Tensor           # bf16 [T, Hkv, D]
+    slot_mapping: np.ndarray      # int64 [T], where each chunk row is stored
+
+    @property
+    def chunk_lens(self) -> np.ndarray:
+        return np.diff(self.query_start_loc)
+
+    @property
+    def max_query_len(self) -> int:
+        return int(self.chunk_lens.max()) if self.chunk_lens.size else 0
+
+    def causal_pairs(self) -> int:
+        """(row, key) pairs one query head attends over: row i of a chunk of n
+        in a sequence of L sees L - n + i + 1 keys."""
+        L = self.wl.context_lens.astype(np.int64)
+        n = self.chunk_lens.astype(np.int64)
+        return int((n * (L - n) + n * (n + 1) // 2).sum())
+
+
+def prefill_batch(spec: Spec, seed: int = 0, chunk=None, context_lens=None,
+                  chunk_lens=None, keep_content: bool = False) -> PrefillBatch:
+    """Draw one prefill step over a pool drawn by ``generate`` (store_mode
+    "none"). ``chunk_lens`` (one per sequence, each <= L_s) overrides
+    ``chunk``."""
+    assert spec.store_mode == "none"
+    wl = generate(spec, seed=seed, context_lens=context_lens, keep_content=keep_content)
+    L = wl.context_lens.astype(np.int64)
+    if chunk_lens is not None:
+        n = np.asarray(chunk_lens, dtype=np.int64)
+    elif chunk is None:
+        n = L.copy()
+    else:
+        n = np.minimum(L, int(chunk))
+    assert n.shape == L.shape and (n >= 0).all() and (n <= L).all()
+    qsl = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    bs = spec.block_size
+    slots = []
+    for s in range(wl.num_seqs):
+        pos = np.arange(L[s] - n[s], L[s])
+        slots.append(wl.block_tables[s, pos // bs].astype(np.int64) * bs + pos % bs)
+    slot_mapping = np.concatenate(slots) if slots else np.zeros(0, np.int64)
+    T = int(qsl[-1])
+    rng = np.random.Generator(np.random.PCG64(seed + 1_000_003))
+    Hq, Hkv, D = spec.num_q_heads, spec.num_kv_heads, spec.head_dim
+    q = _normal_bf16(rng, None, (T, Hq, D), "cpu")
+    k_new = _normal_bf16(rng, None, (T, Hkv, D), "cpu")
+    v_new = _normal_bf16(rng, None, (T, Hkv, D), "cpu")
+    NB = wl.num_blocks
+    nan = float("nan")
+    idx = torch.from_numpy(slot_mapping)
+    wl.k_cache.view(NB * bs, Hkv, D)[idx] = nan
+    wl.v_cache.view(NB * bs, Hkv, D)[idx] = nan
+    return PrefillBatch(wl=wl, query_start_loc=qsl, q=q, k_new=k_new, v_new=v_new,
+                        slot_mapping=slot_mapping)

@@ -32,6 +32,8 @@ SIGNATURES = {
     "pa_decode_noalloc": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                            _I64, _P], _I32),
     "pa_decode_multi_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
+    "pa_prefill": ([_P, _P, _P, _P, _I32, _P, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32, _I32,
+                    _I32, _I64, _P], _I32),
     "pa_store_kvcache_layout": ([_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64, _I32, _P],
                                 _I32),
     "pa_decode_layout": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32, _I64,
@@ -238,6 +240,42 @@ def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out=Non
                                    Hq, Hkv, D, bs, NB, workspace.data_ptr(), ws_bytes,
                                    _stream_ptr(stream, dev))
     _check("pa_decode_multi", st)
+    return out
+
+
+def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale,
+            max_query_len=None, out=None, stream=None):
+    """Paged prefill: q is bf16 [total_q, Hq, D], rows packed per sequence by
+    query_start_loc (int32 [S + 1]); row i of sequence s sits at position
+    context_lens[s] - n_s + i and attends causally to the sequence's cached
+    tokens. Returns out [total_q, Hq, D]."""
+    dev = q.device
+    for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
+                     (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
+                     (context_lens, "context_lens", torch.int32),
+                     (query_start_loc, "query_start_loc", torch.int32)):
+        _cuda(t, n, dt, dev)
+    T, Hq, D = q.shape
+    NB, bs, Hkv, D2 = k_cache.shape
+    S = context_lens.shape[0]
+    if v_cache.shape != k_cache.shape or D2 != D or block_tables.dim() != 2 \
+            or block_tables.shape[0] != S or query_start_loc.shape != (S + 1,):
+        raise ValueError("shape mismatch between q, caches, block_tables and query_start_loc")
+    if max_query_len is None:
+        max_query_len = int((query_start_loc[1:] - query_start_loc[:-1]).max().item()) if S else 0
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda(out, "out", torch.bfloat16, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    with torch.cuda.device(dev):
+        st = lib().pa_prefill(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                              block_tables.data_ptr(), block_tables.shape[1],
+                              context_lens.data_ptr(), query_start_loc.data_ptr(),
+                              int(max_query_len), float(scale), out.data_ptr(), S, T, Hq, Hkv, D,
+                              bs, NB, _stream_ptr(stream, dev))
+    _check("pa_prefill", st)
     return out
 
 

@@ -1,0 +1,161 @@
+"""Paged prefill through the C ABI against the fp64 oracle: each sequence's
+chunk of new rows is stored through its slot mapping, then row i of a chunk of
+n in a sequence of L attends to keys t <= L - n + i."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from paged_kv_cache_255_gb300 import inputs
+from paged_kv_cache_255_gb300 import pagedattn as pa
+
+import gpu_util as gu
+
+pytestmark = pytest.mark.gpu
+PS = inputs.PREFILL_SPECS
+
+
+def _spec(name, Hq, Hkv, bs):
+    return inputs.Spec(name, ((1, 1, 1),), Hq, Hkv, bs, store_mode="none")
+
+
+# (id, spec, chunk, context_lens, chunk_lens)
+CASES = [
+    ("g4_mixed", _spec("a", 8, 2, 16), None, [37, 200, 16, 129, 5], [37, 64, 1, 100, 5]),
+    ("g1_bs32", _spec("b", 8, 8, 32), None, [1, 70, 130, 64], [1, 70, 3, 64]),
+    ("g2_prompts", inputs.scaled(PS["qwen3_0_6b_prompts"][0], num_seqs=6, ctx_div=4), None,
+     None, None),
+    ("g4_chunked", inputs.scaled(PS["chunked_8b"][0], num_seqs=4, ctx_div=16), 100, None, None),
+    ("g8_bs64", _spec("c", 64, 8, 64), None, [300, 77, 129], [150, 77, 65]),
+    ("g16_bs256", _spec("d", 32, 2, 256), None, [520, 33, 1000], [520, 10, 257]),
+    ("g3_pad4", _spec("e", 24, 8, 16), None, [90, 17, 256], [45, 17, 200]),
+    ("g5_pad8", _spec("f", 40, 8, 128), None, [400, 9], [131, 9]),
+    ("empty_chunks", _spec("g", 16, 8, 16), None, [0, 5, 16, 64, 65, 3],
+     [0, 0, 16, 1, 65, 3]),
+]
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib(pa_lib):
+    return pa_lib
+
+
+def _device(pb):
+    wl = pb.wl
+    return dict(
+        q=pb.q.cuda(), k_new=pb.k_new.cuda(), v_new=pb.v_new.cuda(),
+        slot_mapping=torch.from_numpy(pb.slot_mapping).cuda(),
+        k_cache=wl.k_cache.cuda(), v_cache=wl.v_cache.cuda(),
+        block_tables=torch.from_numpy(wl.block_tables).cuda(),
+        context_lens=torch.from_numpy(wl.context_lens).cuda(),
+        qsl=torch.from_numpy(pb.query_start_loc).cuda())
+
+
+def _gpu_step(pb, d, max_query_len=None):
+    """Store the chunk rows, then prefill (the engine's prompt step)."""
+    if pb.slot_mapping.shape[0]:
+        pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+    out = pa.prefill(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                     d["qsl"], pb.wl.scale, max_query_len=max_query_len)
+    torch.cuda.synchronize()
+    return out
+
+
+def _oracle_caches(pb):
+    O = oracle.get()
+    kc, vc = pb.wl.k_cache, pb.wl.v_cache
+    if pb.slot_mapping.shape[0]:
+        kc, vc = O.store_kvcache(pb.k_new, pb.v_new, kc, vc, pb.slot_mapping)
+    return kc, vc
+
+
+@pytest.mark.parametrize("name,spec,chunk,lens,chunks", CASES, ids=[c[0] for c in CASES])
+def test_prefill_matches_oracle(name, spec, chunk, lens, chunks):
+    pb = inputs.prefill_batch(spec, seed=61, chunk=chunk, context_lens=lens, chunk_lens=chunks)
+    kc, vc = _oracle_caches(pb)
+    ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
+                               pb.query_start_loc, pb.wl.scale)
+    d = _device(pb)
+    out = _gpu_step(pb, d)
+    gu.assert_close(out, ref, name)
+    # the store half of the step is byte-exact
+    assert np.array_equal(gu.host_bits(d["k_cache"]), np.asarray(kc))
+    assert np.array_equal(gu.host_bits(d["v_cache"]), np.asarray(vc))
+
+
+def test_small_max_query_len_hint_still_correct():
+    """The hint only sizes the grid: a CTA walks further query tiles itself."""
+    spec = _spec("h", 16, 8, 16)
+    pb = inputs.prefill_batch(spec, seed=62, context_lens=[700, 300], chunk_lens=[650, 300])
+    d = _device(pb)
+    want = _gpu_step(pb, d)
+    got = pa.prefill(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                     d["qsl"], pb.wl.scale, max_query_len=8)
+    torch.cuda.synchronize()
+    assert torch.equal(got.view(torch.int16), want.view(torch.int16))
+
+
+def test_equal_chunks_match_multi_token_decode():
+    """With Q new rows in every sequence, prefill and multi-token decode compute
+    the same attention; both stay within tolerance of the oracle."""
+    spec = _spec("i", 32, 8, 16)
+    Q, lens = 4, [40, 90, 17, 33, 300]
+    pb = inputs.prefill_batch(spec, seed=63, context_lens=lens, chunk_lens=[Q] * len(lens))
+    d = _device(pb)
+    out = _gpu_step(pb, d)
+    multi = pa.decode_multi(d["q"].view(len(lens), Q, 32, 128), d["k_cache"], d["v_cache"],
+                            d["block_tables"], d["context_lens"], pb.wl.scale)
+    torch.cuda.synchronize()
+    kc, vc = _oracle_caches(pb)
+    ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
+                               pb.query_start_loc, pb.wl.scale)
+    gu.assert_close(out, ref, "prefill")
+    gu.assert_close(multi.reshape(out.shape), ref, "decode_multi")
+
+
+def _sampled_rows_ref(pb, kc, vc, rows):
+    """Oracle output of chosen rows: row i of a chunk of n in a sequence of L
+    is a one-row chunk of a sequence cut to its first L - n + i + 1 tokens."""
+    qsl = pb.query_start_loc
+    seq = np.searchsorted(qsl, rows, side="right") - 1
+    n = qsl[seq + 1] - qsl[seq]
+    i = rows - qsl[seq]
+    L = pb.wl.context_lens[seq].astype(np.int64)
+    cut = (L - n + i + 1).astype(np.int32)
+    one = np.arange(len(rows) + 1, dtype=np.int32)
+    return oracle.get().prefill(pb.q[torch.from_numpy(rows)], kc, vc,
+                                pb.wl.block_tables[seq], cut, one, pb.wl.scale)
+
+
+@pytest.mark.parametrize("name", sorted(PS))
+def test_full_size_sampled_rows(name):
+    """The benchmarked prefill steps at full size, in the benchmark's launch
+    configuration; the oracle checks a sample of rows one by one (the first and
+    last rows of the first 16 chunks and 32 random rows)."""
+    spec, chunk = PS[name]
+    pb = inputs.prefill_batch(spec, seed=0, chunk=chunk)
+    d = _device(pb)
+    out = _gpu_step(pb, d, max_query_len=pb.max_query_len)
+    qsl = pb.query_start_loc
+    rng = np.random.Generator(np.random.PCG64(64))
+    firsts = qsl[:-1][np.diff(qsl) > 0]
+    lasts = qsl[1:][np.diff(qsl) > 0] - 1
+    rows = np.unique(np.concatenate([firsts[:16], lasts[:16],
+                                     rng.integers(0, qsl[-1], size=32)])).astype(np.int64)
+    kc = d["k_cache"].cpu()
+    vc = d["v_cache"].cpu()
+    ref = _sampled_rows_ref(pb, kc, vc, rows)
+    gu.assert_close(out[torch.from_numpy(rows).cuda()], ref, name)
+    assert torch.isfinite(out.float()).all()
+
+
+def test_rejects_bad_shapes():
+    spec = _spec("j", 16, 8, 16)
+    pb = inputs.prefill_batch(spec, seed=65, context_lens=[20], chunk_lens=[20])
+    d = _device(pb)
+    with pytest.raises(ValueError):
+        pa.prefill(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                   d["qsl"][:1], pb.wl.scale)
+    with pytest.raises(pa.PagedAttnError):      # 12 query heads over 8 KV heads
+        pa.prefill(d["q"][:, :12].contiguous(), d["k_cache"], d["v_cache"],
+                   d["block_tables"], d["context_lens"], d["qsl"], pb.wl.scale)
