@@ -261,6 +261,17 @@ PA_API pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_
                               int total_q, int num_q_heads, int num_kv_heads, int head_dim,
                               int block_size, int64_t num_blocks, void *stream);
 
+/*
+ * Device-side error check for pa_prefill. The prefill kernel waits on the
+ * tensor cores through mbarriers, each wait bounded (about 2 s); a wait that
+ * runs out, or shared memory the kernel cannot align, is recorded on the
+ * device instead of hanging. This call synchronizes `stream`, stores the first
+ * recorded code in *code (0 = none, 1 = shared memory misaligned, 2 = a wait
+ * ran out; the outputs of the affected launch are then undefined) and clears
+ * it.
+ */
+PA_API pa_status_t pa_take_device_error(int32_t *code, void *stream);
+
 #ifdef __cplusplus
 }
 #endif

@@ -255,9 +255,21 @@ pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.num_blocks = num_blocks;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
-    const cudaError_t e = pa::launch_prefill(a, gp, max_query_len > 0 ? max_query_len : 1,
-                                             static_cast<cudaStream_t>(stream));
+    const int mql = max_query_len > 0 ? max_query_len : 1;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const char *k = std::getenv("PA_PREFILL_KERNEL");
+    const cudaError_t e = (k && std::strcmp(k, "mma") == 0) ? pa::launch_prefill(a, gp, mql, st)
+                                                            : pa::launch_prefill_tc(a, gp, mql, st);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status_t pa_take_device_error(int32_t *code, void *stream) {
+    if (!code) return PA_ERR_INVALID_ARG;
+    int v = 0;
+    if (pa::take_prefill_error(static_cast<cudaStream_t>(stream), &v) != cudaSuccess)
+        return PA_ERR_CUDA;
+    *code = v;
+    return PA_OK;
 }
 
 }  // extern "C"

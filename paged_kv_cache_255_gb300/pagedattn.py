@@ -34,6 +34,7 @@ SIGNATURES = {
     "pa_decode_multi_workspace_size": ([_I32, _I32, _I32, _I32], _SZ),
     "pa_prefill": ([_P, _P, _P, _P, _I32, _P, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                     _I32, _I64, _P], _I32),
+    "pa_take_device_error": ([_P, _P], _I32),
     "pa_store_kvcache_layout": ([_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64, _I32, _P],
                                 _I32),
     "pa_decode_layout": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32, _I64,
@@ -277,6 +278,18 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, sc
                               bs, NB, _stream_ptr(stream, dev))
     _check("pa_prefill", st)
     return out
+
+
+def take_device_error(stream=None, device=None) -> int:
+    """Synchronize the stream and return (and clear) the first device-side
+    error code a prefill launch recorded: 0 none, 1 shared memory misaligned,
+    2 a tensor-core wait ran out."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else device
+    code = ctypes.c_int32(0)
+    with torch.cuda.device(dev):
+        st = lib().pa_take_device_error(ctypes.addressof(code), _stream_ptr(stream, dev))
+    _check("pa_take_device_error", st)
+    return int(code.value)
 
 
 class DecodeStepGraph:

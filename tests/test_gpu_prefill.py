@@ -69,22 +69,37 @@ def _oracle_caches(pb):
     return kc, vc
 
 
+@pytest.fixture(autouse=True)
+def _no_device_error():
+    assert pa.take_device_error() == 0
+    yield
+    assert pa.take_device_error() == 0, "a prefill launch recorded a device-side error"
+
+
+# tc: tcgen05 with TMEM accumulators (the default); mma: the mma.sync kernel
+KERNELS = ["tc", "mma"]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name,spec,chunk,lens,chunks", CASES, ids=[c[0] for c in CASES])
-def test_prefill_matches_oracle(name, spec, chunk, lens, chunks):
+def test_prefill_matches_oracle(name, spec, chunk, lens, chunks, kernel, monkeypatch):
+    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
     pb = inputs.prefill_batch(spec, seed=61, chunk=chunk, context_lens=lens, chunk_lens=chunks)
     kc, vc = _oracle_caches(pb)
     ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
                                pb.query_start_loc, pb.wl.scale)
     d = _device(pb)
     out = _gpu_step(pb, d)
-    gu.assert_close(out, ref, name)
+    gu.assert_close(out, ref, f"{name} ({kernel})")
     # the store half of the step is byte-exact
     assert np.array_equal(gu.host_bits(d["k_cache"]), np.asarray(kc))
     assert np.array_equal(gu.host_bits(d["v_cache"]), np.asarray(vc))
 
 
-def test_small_max_query_len_hint_still_correct():
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_small_max_query_len_hint_still_correct(kernel, monkeypatch):
     """The hint only sizes the grid: a CTA walks further query tiles itself."""
+    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
     spec = _spec("h", 16, 8, 16)
     pb = inputs.prefill_batch(spec, seed=62, context_lens=[700, 300], chunk_lens=[650, 300])
     d = _device(pb)
@@ -125,6 +140,22 @@ def _sampled_rows_ref(pb, kc, vc, rows):
     one = np.arange(len(rows) + 1, dtype=np.int32)
     return oracle.get().prefill(pb.q[torch.from_numpy(rows)], kc, vc,
                                 pb.wl.block_tables[seq], cut, one, pb.wl.scale)
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+def test_negative_scale(kernel, monkeypatch):
+    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
+    spec = _spec("k", 16, 8, 16)
+    pb = inputs.prefill_batch(spec, seed=66, context_lens=[150, 40], chunk_lens=[100, 40])
+    kc, vc = _oracle_caches(pb)
+    ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
+                               pb.query_start_loc, -0.3)
+    d = _device(pb)
+    pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+    out = pa.prefill(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                     d["qsl"], -0.3)
+    torch.cuda.synchronize()
+    gu.assert_close(out, ref, f"negative scale ({kernel})")
 
 
 @pytest.mark.parametrize("name", sorted(PS))
