@@ -3,34 +3,49 @@
 // tokens in the paged KV cache; "A vLLM engine small enough to read in one
 // sitting": prefill and decode run over the paged KV cache, flash attention
 // for prefill), computed in the flash-attention order with the two
-// contractions on tcgen05.mma and both accumulators in tensor memory.
+// contractions on tcgen05.mma and all accumulators in tensor memory.
 //
-// A CTA of 4 warps owns 128 rows of one (sequence, KV head): 128 / G query
-// tokens x the G query heads of the group (G = group size rounded up to a
-// power of two); thread t owns row t, which is TMEM lane t. Per 64-key tile j:
-//   S = Q K_j^T   M 128, N 64, K 128: Q and K_j in shared memory, S in TMEM
-//   softmax       each thread reads its row of S (tcgen05.ld), masks it
-//                 causally, updates its running max / sum and writes P (bf16)
-//                 to shared memory
-//   O += P V_j    M 128, N 128, K 64: P and V_j in shared memory, O in TMEM
+// One CTA per SM owns two 128-row query tiles A and B of one (sequence, KV
+// head); a tile is 128 / G query tokens x the G query heads of the group (G =
+// group size rounded up to a power of two), so every K/V tile fetched serves
+// 256 rows. Warp roles:
+//   warps 0-3, 4-7   softmax of tile A, B: thread t of the warpgroup owns row
+//                    t, which is TMEM lane t. Per 64-key tile j it reads its
+//                    row of S_j (tcgen05.ld), masks it causally, updates its
+//                    running max and sum, writes P_j (bf16) to shared memory.
+//   warps 8, 9       K and V producers: per 64-key tile, 8 lanes each fetch
+//                    16-token boxes of one KV head by TMA through a 3-D tensor
+//                    map over the pool ([NB * bs, Hkv, 128]), landing in the
+//                    128-byte swizzled layout the MMA descriptors name, into
+//                    4-stage rings. A K stage is refilled as soon as both S
+//                    of its tile are done, a V stage after both PV. V rows of
+//                    a partly used 16-token group at the end of the keys are
+//                    copied (and the rows past the end zeroed) by the lanes.
+//   warp 10          Q producer: both query tiles, by 16-byte cp.async.
+//   warp 11          issues the MMAs (one elected lane), S_t(j) = Q_t K_j^T and
+//                    O_t += P_t(j) V_j for t in {A, B}, each as soon as its
+//                    inputs are ready (S_t(j + 1) is computed while the
+//                    softmax works on S_t(j)); 16-token groups of V wholly
+//                    past the end of the keys are left out of PV.
 // The running max is raised only when a tile's max exceeds it by more than
 // 2^8 (in exp2 units); otherwise the stale max is kept, which changes nothing
-// in O / l but the rounding, and saves reading and writing O back. When it is
-// raised, the warp rescales its rows of O in TMEM.
+// in O / l but the rounding. When it is raised, the warp rescales its rows of
+// O in TMEM before the next PV.
 //
-// Thread 0 issues the MMAs; tcgen05.commit signals their completion on two
-// mbarriers (S done, PV done). K and V tiles are gathered through the block
-// table by 16-byte cp.async into two-stage rings, written in the 128-byte
-// swizzled layout the MMA descriptors name. K_{j+2} is fetched as soon as
-// S_j has finished with K_j's stage, V_{j+1} as soon as PV_{j-1} has finished
-// with its stage. Two CTAs share an SM (115 KB shared memory and 256 TMEM
-// columns each), so one CTA's softmax overlaps the other's MMAs.
-//
-// Every mbarrier wait is bounded (about 2 s); a CTA whose wait runs out
-// records an error, stops at the next CTA-wide barrier (all threads learn of it
-// there through __syncthreads_or), waits for its copies, frees its TMEM and
-// exits.
+// Hand-offs are mbarriers: k_full / v_full complete when the TMA bytes have
+// landed and the producer warp has arrived (after fencing its own
+// shared-memory writes to the async proxy); q_full when the Q warp's copies have landed and been
+// fenced; tcgen05.commit arrives on
+// s_full, pv_done, k_empty and v_empty; the softmax threads arrive on s_free once
+// their row of S is in registers and on p_ready once P is in shared memory
+// (and O rescaled). Every wait is bounded (about 2 s) and also gives up once
+// any thread of the CTA has recorded a failed wait; then every role skips to
+// the end, where the CTA frees its TMEM and exits.
 #include <cmath>
+#include <mutex>
+
+#include <cuda.h>
+#include <cudaTypedefs.h>
 
 #include "common.cuh"
 #include "kernels.h"
@@ -42,22 +57,44 @@ __device__ int g_prefill_error;      // first device-side error of a prefill lau
 
 namespace {
 
-constexpr int kRows = 128;
-constexpr int kKeys = 64;
-constexpr int kThreads = 128;
+constexpr int kRows = 128;                              // rows per query tile
+constexpr int kKeys = 64;                               // keys per K/V tile
+constexpr int kStages = 4;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kKWarp = kSoftmaxThreads / 32;             // 8
+constexpr int kVWarp = kKWarp + 1;                       // 9
+constexpr int kQWarp = kKWarp + 2;                       // 10
+constexpr int kMmaWarp = kKWarp + 3;                     // 11
+constexpr int kThreads = kSoftmaxThreads + 4 * 32;
+constexpr int kGroup = 16;                               // tokens per TMA box
 constexpr uint32_t kQBytes = kRows * kRowBytes;         // 32 KB: 2 K-halves of [128][128 B]
 constexpr uint32_t kQHalf = kRows * 128;                // 16 KB
 constexpr uint32_t kKVBytes = kKeys * kRowBytes;        // 16 KB: 2 halves of [64][128 B]
 constexpr uint32_t kKVHalf = kKeys * 128;               // 8 KB
 constexpr uint32_t kPBytes = kRows * kKeys * 2;         // 16 KB: [128][128 B]
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kQBytes;             // 2 stages
-constexpr uint32_t kOffV = kOffK + 2 * kKVBytes;        // 2 stages
-constexpr uint32_t kOffP = kOffV + 2 * kKVBytes;
-constexpr uint32_t kOffCtl = kOffP + kPBytes;           // mbarriers, TMEM base, abort flag
-constexpr uint32_t kSmemBytes = kOffCtl + 64;
-constexpr uint32_t kTmemCols = 256;                     // S: columns 0-63, O: 128-255
-constexpr uint32_t kColO = 128;
+constexpr uint32_t kOffQ = 0;                           // Q_A, Q_B
+constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;         // P_A, P_B
+constexpr uint32_t kOffKV = kOffP + 2 * kPBytes;        // stage i: K at i * 32 KB, V 16 KB on
+constexpr uint32_t kOffCtl = kOffKV + kStages * 2 * kKVBytes;
+// control block: mbarriers (8 B each), then the TMEM base and the abort flag
+constexpr uint32_t kBarQFull = 0;
+constexpr uint32_t kBarQEmpty = 1;
+constexpr uint32_t kBarKFull = 2;                       // + stage
+constexpr uint32_t kBarKEmpty = kBarKFull + kStages;    // + stage
+constexpr uint32_t kBarVFull = kBarKEmpty + kStages;    // + stage
+constexpr uint32_t kBarVEmpty = kBarVFull + kStages;    // + stage
+constexpr uint32_t kBarSFull = kBarVEmpty + kStages;    // + tile (A 0, B 1)
+constexpr uint32_t kBarSFree = kBarSFull + 2;
+constexpr uint32_t kBarPReady = kBarSFree + 2;
+constexpr uint32_t kBarPVDone = kBarPReady + 2;
+constexpr uint32_t kBarOFree = kBarPVDone + 2;
+constexpr uint32_t kNumBars = kBarOFree + 2;
+constexpr uint32_t kOffTmemSlot = kOffCtl + 8 * kNumBars;
+constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
+constexpr uint32_t kSmemBytes = kOffCtl + 256;
+static_assert(kOffAbort + 4 <= kSmemBytes, "control block");
+// TMEM: S_A 0-63, S_B 64-127, O_A 128-255, O_B 256-383
+constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, kKeys, false);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, true);
 constexpr float kRescaleSlack = 8.f;                    // log2 units
@@ -66,35 +103,111 @@ enum : int { kErrSmemAlign = 1, kErrTimeout = 2 };
 
 __device__ __forceinline__ void set_error(int code) { atomicCAS(&g_prefill_error, 0, code); }
 
-// cp.async of K or V rows of keys [k0, k0 + 64) of (sequence s, KV head kvh)
-// into a stage: key r, 16-byte chunk c (dims 8c..8c+7) goes to half c / 8,
-// row r, chunk position (c % 8) ^ (r % 8). Keys at or past kend are zero.
-__device__ __forceinline__ void load_kv(const PrefillArgs &a, const void *cache, int s, int kvh,
-                                        int k0, int kend, uint32_t stage) {
-    const int bs_mask = (1 << a.block_size_log2) - 1;
-    const char *base = static_cast<const char *>(cache);
-#pragma unroll
-    for (int i = 0; i < (kKeys * 16) / kThreads; ++i) {
-        const int c = threadIdx.x + i * kThreads;
-        const int key = c >> 4, chunk = c & 15;
-        const int t = k0 + key;
-        bool ok = t < kend;
-        int64_t row = 0;
-        if (ok) {
-            const int bid = __ldg(a.block_tables + (int64_t)s * a.max_blocks_per_seq +
-                                  (t >> a.block_size_log2));
-            ok = bid >= 0 && (int64_t)bid < a.num_blocks;
-            row = (((int64_t)bid << a.block_size_log2) + (t & bs_mask)) * a.num_kv_heads + kvh;
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+
+// Bounded wait that also gives up once the CTA's abort flag is set. Between
+// checks the thread sleeps in the barrier (woken when the phase completes), so
+// that waiting warps leave shared-memory bandwidth to the tensor core.
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort) {
+    if (tc::mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = tc::globaltimer_ns();
+    for (;;) {
+        if (tc::mbar_try_wait_sleep(bar, parity, 100000u)) return true;
+        if (*abort) return false;
+        if (tc::globaltimer_ns() - t0 > 2000000000ull) {
+            set_error(kErrTimeout);
+            *abort = 1;
+            return false;
         }
-        const uint32_t dst = stage + (chunk >> 3) * kKVHalf + key * 128 +
-                             ((((uint32_t)chunk & 7) ^ ((uint32_t)key & 7)) << 4);
-        cp_async_16(dst, base + (ok ? row * kRowBytes + chunk * 16 : 0), ok ? 16 : 0);
     }
 }
 
+// Warp-level hand-offs: one lane waits (or arrives) for the whole warp, the
+// others are ordered with it by __syncwarp. Fewer arrivals and polls on the
+// barrier words leave shared memory to the tensor core's operand reads.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+    bool ok = true;
+    if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort);
+    const bool r = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return r;
+}
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
+// Physical row (token slot) of key t of sequence s in the pool, or -1.
+__device__ __forceinline__ int64_t key_row(const PrefillArgs &a, int s, int t) {
+    const int bid = __ldg(a.block_tables + (int64_t)s * a.max_blocks_per_seq + (t >> a.block_size_log2));
+    if (bid < 0 || (int64_t)bid >= a.num_blocks) return -1;
+    return ((int64_t)bid << a.block_size_log2) + (t & ((1 << a.block_size_log2) - 1));
+}
+
+// The V rows of the 16-token group starting at key t0 (which holds the end
+// kend of the keys) into its place in a V stage, by the 32 lanes of a warp;
+// rows at or past kend are zero. Plain loads and shared stores.
+__device__ __forceinline__ void copy_v_tail(const PrefillArgs &a, int s, int kvh, int t0, int kend,
+                                            uint32_t vdst, int lane) {
+    const int chunk = lane & 15;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const int r = (lane >> 4) + 2 * i;          // row of the group
+        const int t = t0 + r;
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (t < kend) {
+            const int64_t row = key_row(a, s, t);
+            if (row >= 0)
+                w = __ldg(reinterpret_cast<const uint4 *>(
+                    static_cast<const char *>(a.v_cache) +
+                    (row * a.num_kv_heads + kvh) * kRowBytes + chunk * 16));
+        }
+        const int key = (t0 & (kKeys - 1)) + r;     // row in the tile
+        const uint32_t dst = vdst + (chunk >> 3) * kKVHalf + key * 128 +
+                             ((((uint32_t)chunk & 7) ^ ((uint32_t)key & 7)) << 4);
+        asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst), "r"(w.x), "r"(w.y),
+                     "r"(w.z), "r"(w.w)
+                     : "memory");
+    }
+}
+
+// 16-token groups of the tile at k0 that hold keys (first key < kend), and
+// those wholly below kend.
+__device__ __forceinline__ int groups_used(int k0, int kend) {
+    const int n = (kend - k0 + kGroup - 1) / kGroup;
+    return n < 0 ? 0 : (n > kKeys / kGroup ? kKeys / kGroup : n);
+}
+__device__ __forceinline__ int groups_full(int k0, int kend) {
+    const int n = (kend - k0) / kGroup;
+    return n < 0 ? 0 : (n > kKeys / kGroup ? kKeys / kGroup : n);
+}
+
+// Work item: a pair of query tiles (2 x 128 / G tokens) of one (sequence, KV
+// head). Every role walks the same items and computes the same bounds.
+struct Item {
+    int tok0;       // first token of tile A
+    int nt;         // K/V tiles the pair reads
+};
+
 template <int G>
-__global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillArgs a) {
-    constexpr int BT = kRows / G;               // query tokens per CTA tile
+__device__ __forceinline__ Item make_item(int qp, int n, int L) {
+    constexpr int BT = kRows / G;
+    Item it;
+    it.tok0 = qp * 2 * BT;
+    const int last_tok = (it.tok0 + 2 * BT < n ? it.tok0 + 2 * BT : n) - 1;
+    int kend = L - n + last_tok + 1;
+    kend = kend < 0 ? 0 : (kend > L ? L : kend);
+    it.nt = (kend + kKeys - 1) / kKeys;
+    return it;
+}
+
+template <int G>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
+                  const __grid_constant__ CUtensorMap tmap_v) {
+    constexpr int BT = kRows / G;               // query tokens per query tile
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5;
     const int s = blockIdx.y, kvh = blockIdx.z;
@@ -105,9 +218,10 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillAr
     q0 = q0 < 0 ? 0 : (q0 > a.total_q ? a.total_q : q0);
     q1 = q1 < q0 ? q0 : (q1 > a.total_q ? a.total_q : q1);
     const int n = q1 - q0;
-    // heaviest tiles (last rows of the chunk see the most keys) first
-    const int qt_first = gridDim.x - 1 - blockIdx.x;
-    if (qt_first * BT >= n) return;
+    // pairs qp_first, qp_first + gridDim.x, ...; the heaviest (last rows of
+    // the chunk see the most keys) first
+    const int qp_first = gridDim.x - 1 - blockIdx.x;
+    if (qp_first * 2 * BT >= n) return;
 
     const uint32_t sbase = smem_u32(smem);
     if (sbase & 1023u) {                        // the swizzle atoms need 1024-byte alignment
@@ -119,227 +233,420 @@ __global__ void __launch_bounds__(kThreads, 2) prefill_tc_kernel(const PrefillAr
         const int64_t max_len = (int64_t)a.max_blocks_per_seq << a.block_size_log2;
         L = L < 0 ? 0 : ((int64_t)L > max_len ? (int)max_len : L);
     }
-    const uint32_t sQ = sbase + kOffQ, sK = sbase + kOffK, sV = sbase + kOffV, sP = sbase + kOffP;
-    const uint32_t bar_s = sbase + kOffCtl, bar_pv = bar_s + 8;
-    volatile uint32_t *tmem_slot = reinterpret_cast<volatile uint32_t *>(smem + kOffCtl + 16);
+    // kend of a pair: L - n + (its last token) + 1
+    auto kend_of = [&](const Item &it) {
+        const int last_tok = (it.tok0 + 2 * BT < n ? it.tok0 + 2 * BT : n) - 1;
+        const int k = L - n + last_tok + 1;
+        return k < 0 ? 0 : (k > L ? L : k);
+    };
 
+    const uint32_t ctl = sbase + kOffCtl;
+    auto bar = [&](uint32_t i) { return ctl + 8 * i; };
+    volatile int *abort = reinterpret_cast<volatile int *>(smem + kOffAbort);
     if (tid == 0) {
-        tc::mbar_init(bar_s, 1);
-        tc::mbar_init(bar_pv, 1);
+        tc::mbar_init(bar(kBarQFull), 1);
+        tc::mbar_init(bar(kBarQEmpty), 1);
+        for (int i = 0; i < kStages; ++i) {
+            tc::mbar_init(bar(kBarKFull + i), 1);
+            tc::mbar_init(bar(kBarKEmpty + i), 1);
+            tc::mbar_init(bar(kBarVFull + i), 1);
+            tc::mbar_init(bar(kBarVEmpty + i), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            tc::mbar_init(bar(kBarSFull + i), 1);
+            tc::mbar_init(bar(kBarSFree + i), kRows / 32);
+            tc::mbar_init(bar(kBarPReady + i), kRows / 32);
+            tc::mbar_init(bar(kBarPVDone + i), 1);
+            tc::mbar_init(bar(kBarOFree + i), kRows / 32);
+        }
+        *abort = 0;
         tc::fence_mbar_init();
     }
-    if (warp == 0) tc::tmem_alloc(sbase + kOffCtl + 16, kTmemCols);
+    if (warp == kMmaWarp) tc::tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
     tc::fence_before_sync();
     __syncthreads();
     tc::fence_after_sync();
-    const uint32_t tmem = *tmem_slot;
-    const uint32_t lane = (uint32_t)(warp * 32) << 16;       // this warp's TMEM lane quarter
-    const uint32_t tS = tmem, tO = tmem + kColO;
-    uint32_t ph_s = 0, ph_pv = 0;
-    bool aborted = false;          // CTA-uniform: set from __syncthreads_or
-    int timed_out = 0;             // this thread's waits
+    const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + kOffTmemSlot);
 
-    const uint16_t *qg = static_cast<const uint16_t *>(a.q);
-    char *outg = static_cast<char *>(a.out);
-
-#pragma unroll 1
-    for (int qt = qt_first; qt * BT < n && !aborted; qt += gridDim.x) {
-        const int tok0 = qt * BT;
-        const int tok = tok0 + tid / G, head = tid % G;
-        const bool rv = tok < n && head < g;
-        int lim = 0;
-        if (rv) {
-            const int l = L - n + tok + 1;
-            lim = l < 0 ? 0 : (l > L ? L : l);
-        }
-        const int last_tok = (tok0 + BT < n ? tok0 + BT : n) - 1;
-        int kend = L - n + last_tok + 1;
-        kend = kend < 0 ? 0 : (kend > L ? L : kend);
-        const int ntiles = (kend + kKeys - 1) / kKeys;
-        const int64_t row_elem = ((int64_t)q0 + tok) * a.num_q_heads + (int64_t)kvh * g + head;
-
-        // Q row -> shared (K-major, swizzled), K_0 / V_0, then K_1
-        {
-            const char *src = reinterpret_cast<const char *>(qg + (rv ? row_elem : 0) * kHeadDim);
-#pragma unroll
-            for (int c = 0; c < 16; ++c) {
-                const uint32_t dst = sQ + (c >> 3) * kQHalf + tid * 128 +
-                                     ((((uint32_t)c & 7) ^ ((uint32_t)tid & 7)) << 4);
-                cp_async_16(dst, src + (rv ? c * 16 : 0), rv ? 16 : 0);
-            }
-        }
-        if (ntiles > 0) {
-            load_kv(a, a.k_cache, s, kvh, 0, kend, sK);
-            load_kv(a, a.v_cache, s, kvh, 0, kend, sV);
-        }
-        cp_async_commit();
-        if (ntiles > 1) load_kv(a, a.k_cache, s, kvh, kKeys, kend, sK + kKVBytes);
-        cp_async_commit();
-        cp_async_wait<1>();
-        tc::fence_proxy_async();
-        tc::fence_before_sync();
-        __syncthreads();
-
-        auto issue_s = [&](int stage) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int k = 0; k < kHeadDim / 16; ++k) {
-                const uint32_t off = (k & 3) * 32;
-                tc::mma_ss(tS, tc::sw128_desc(sQ + (k >> 2) * kQHalf + off, 16, 1024),
-                           tc::sw128_desc(sK + stage * kKVBytes + (k >> 2) * kKVHalf + off, 16, 1024),
-                           kIdescS, k > 0);
-            }
-            tc::commit(bar_s);
-        };
-        auto issue_pv = [&](int stage, bool acc) {
-            tc::fence_after_sync();
-#pragma unroll
-            for (int k = 0; k < kKeys / 16; ++k)
-                tc::mma_ss(tO, tc::sw128_desc(sP + k * 32, 16, 1024),
-                           tc::sw128_desc(sV + stage * kKVBytes + k * 2048, kKVHalf, 1024),
-                           kIdescPV, acc || k > 0);
-            tc::commit(bar_pv);
-        };
-        if (tid == 0 && ntiles > 0) issue_s(0);
-
-        float m = -INFINITY, lsum = 0.f;
+    if (tid < kSoftmaxThreads) {
+        // ---------------- softmax warpgroups ----------------
+        const int wg = tid >> 7, r = tid & 127;
+        const uint32_t lane = (uint32_t)(r & ~31) << 16;
+        const uint32_t tS = tmem + wg * kKeys, tO = tmem + 128 + wg * 128;
+        const uint32_t sP = sbase + kOffP + wg * kPBytes;
         const float sc = a.scale_log2;
+        uint32_t gt = 0;                        // tiles done before this item
+        bool ok = true;
 #pragma unroll 1
-        for (int j = 0; j < ntiles; ++j) {
-            // 1. this row of S_j
-            if (!tc::mbar_wait(bar_s, ph_s)) { set_error(kErrTimeout); timed_out = 1; }
-            ph_s ^= 1;
-            tc::fence_after_sync();
-            uint32_t sr[2][32];
-            tc::tmem_ld32(tS + lane, sr[0]);
-            tc::tmem_ld32(tS + lane + 32, sr[1]);
-            tc::tmem_ld_wait();
-            // K_j's stage is free: fetch K_{j+2} into it
-            if (j + 2 < ntiles) load_kv(a, a.k_cache, s, kvh, (j + 2) * kKeys, kend, sK + (j & 1) * kKVBytes);
-            cp_async_commit();
-
-            // 2. scores in exp2 units, causal mask, running max (raised
-            // lazily), P = 2^(S sc - m)
-            const int kb = j * kKeys;
-            float mt = -INFINITY;
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int c = 0; c < 32; ++c) {
-                    float v = __uint_as_float(sr[h][c]) * sc;
-                    if (kb + h * 32 + c >= lim) v = -INFINITY;
-                    sr[h][c] = __float_as_uint(v);
-                    mt = fmaxf(mt, v);
-                }
-            bool rescale = false;
-            float alpha = 1.f;
-            if (mt > m + kRescaleSlack) {
-                rescale = m != -INFINITY;
-                alpha = rescale ? ex2(m - mt) : 1.f;
-                lsum *= alpha;
-                m = mt;
+        for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x) {
+            const Item it = make_item<G>(qp, n, L);
+            const int tok = it.tok0 + wg * BT + r / G, head = r % G;
+            const bool rv = tok < n && head < g;
+            int lim = 0;
+            if (rv) {
+                const int l = L - n + tok + 1;
+                lim = l < 0 ? 0 : (l > L ? L : l);
             }
-            const float mb = m == -INFINITY ? 0.f : m;
-            uint32_t pw[32];
-#pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int c = 0; c < 16; ++c) {
-                    const float p0 = ex2(__uint_as_float(sr[h][2 * c]) - mb);
-                    const float p1 = ex2(__uint_as_float(sr[h][2 * c + 1]) - mb);
-                    const uint32_t w = pack_bf16x2(p0, p1);
-                    lsum += bf16_lo(w) + bf16_hi(w);
-                    pw[h * 16 + c] = w;
-                }
+            float m = -INFINITY, lsum = 0.f;
+#pragma unroll 1
+            for (int j = 0; j < it.nt; ++j) {
+                const uint32_t gj = gt + j;
+                if (!warp_wait(bar(kBarSFull + wg), gj & 1, abort)) { ok = false; break; }
+                tc::fence_after_sync();
+                uint32_t sr[2][32];
+                tc::tmem_ld32(tS + lane, sr[0]);
+                tc::tmem_ld32(tS + lane + 32, sr[1]);
+                tc::tmem_ld_wait();
+                tc::fence_before_sync();
+                warp_arrive(bar(kBarSFree + wg));
 
-            // 3. PV_{j-1} done: O is stable, P and V_{j-1}'s stage are free
-            if (j > 0) {
-                if (!tc::mbar_wait(bar_pv, ph_pv)) { set_error(kErrTimeout); timed_out = 1; }
-                ph_pv ^= 1;
+                // scores in exp2 units, causal mask, lazily raised max,
+                // P = 2^(S sc - m)
+                const int kb = j * kKeys;
+                float mt = -INFINITY;
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int c = 0; c < 32; ++c) {
+                        float v = __uint_as_float(sr[h][c]) * sc;
+                        if (kb + h * 32 + c >= lim) v = -INFINITY;
+                        sr[h][c] = __float_as_uint(v);
+                        mt = fmaxf(mt, v);
+                    }
+                bool rescale = false;
+                float alpha = 1.f;
+                if (mt > m + kRescaleSlack) {
+                    rescale = m != -INFINITY;
+                    alpha = rescale ? ex2(m - mt) : 1.f;
+                    lsum *= alpha;
+                    m = mt;
+                }
+                const float mb = m == -INFINITY ? 0.f : m;
+                uint32_t pw[32];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int c = 0; c < 16; ++c) {
+                        const float p0 = ex2(__uint_as_float(sr[h][2 * c]) - mb);
+                        const float p1 = ex2(__uint_as_float(sr[h][2 * c + 1]) - mb);
+                        const uint32_t w = pack_bf16x2(p0, p1);
+                        lsum += bf16_lo(w) + bf16_hi(w);
+                        pw[h * 16 + c] = w;
+                    }
+
+                // PV(j-1) done: O stable, P buffer free
+                if (j > 0) {
+                    if (!warp_wait(bar(kBarPVDone + wg), (gj - 1) & 1, abort)) { ok = false; break; }
+                    tc::fence_after_sync();
+                }
+                if (__any_sync(0xffffffffu, rescale)) {
+#pragma unroll 1
+                    for (int ch = 0; ch < 4; ++ch) {
+                        uint32_t o[32];
+                        tc::tmem_ld32(tO + lane + ch * 32, o);
+                        tc::tmem_ld_wait();
+#pragma unroll
+                        for (int c = 0; c < 32; ++c)
+                            o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
+                        tc::tmem_st32(tO + lane + ch * 32, o);
+                    }
+                    tc::tmem_st_wait();
+                }
+#pragma unroll
+                for (int c = 0; c < 8; ++c) {
+                    const uint32_t dst = sP + r * 128 + ((((uint32_t)c) ^ ((uint32_t)r & 7)) << 4);
+                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst),
+                                 "r"(pw[4 * c]), "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]),
+                                 "r"(pw[4 * c + 3])
+                                 : "memory");
+                }
+                tc::fence_proxy_async();
+                tc::fence_before_sync();
+                warp_arrive(bar(kBarPReady + wg));
+            }
+            if (!ok) break;
+            // epilogue: O / l -> bf16 rows; then O is free for the next item
+            if (it.nt > 0) {
+                if (!warp_wait(bar(kBarPVDone + wg), (gt + it.nt - 1) & 1, abort)) { ok = false; break; }
                 tc::fence_after_sync();
             }
-            if (j + 1 < ntiles) load_kv(a, a.v_cache, s, kvh, (j + 1) * kKeys, kend, sV + ((j + 1) & 1) * kKVBytes);
-            cp_async_commit();
-
-            // 4. rescale this warp's rows of O if any of them raised its max
-            if (__any_sync(0xffffffffu, rescale)) {
+            const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
+            const int64_t row_elem = ((int64_t)q0 + tok) * a.num_q_heads + (int64_t)kvh * g + head;
+            uint4 *orow = reinterpret_cast<uint4 *>(static_cast<char *>(a.out) + row_elem * kRowBytes);
 #pragma unroll 1
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t o[32];
+            for (int ch = 0; ch < 4; ++ch) {
+                uint32_t o[32];
+                if (it.nt > 0) {
                     tc::tmem_ld32(tO + lane + ch * 32, o);
                     tc::tmem_ld_wait();
+                } else {
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                    tc::tmem_st32(tO + lane + ch * 32, o);
+                    for (int c = 0; c < 32; ++c) o[c] = 0u;
                 }
-                tc::tmem_st_wait();
-            }
-
-            // 5. P_j -> shared (row tid, K-major, swizzled)
+                if (rv) {
 #pragma unroll
-            for (int c = 0; c < 8; ++c) {
-                const uint32_t dst = sP + tid * 128 + ((((uint32_t)c) ^ ((uint32_t)tid & 7)) << 4);
-                asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst),
-                             "r"(pw[4 * c]), "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]), "r"(pw[4 * c + 3])
-                             : "memory");
+                    for (int c = 0; c < 4; ++c) {
+                        uint4 w;
+                        w.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
+                        w.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
+                        w.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
+                        w.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
+                        orow[ch * 4 + c] = w;
+                    }
+                }
             }
-            // 6. K_{j+1} and V_j have landed (two newer groups may be pending)
-            cp_async_wait<2>();
-            tc::fence_proxy_async();
             tc::fence_before_sync();
-            if (__syncthreads_or(timed_out)) { aborted = true; break; }
-            // 7. O += P_j V_j, then S_{j+1} = Q K_{j+1}^T
-            if (tid == 0) {
-                issue_pv(j & 1, j > 0);
-                if (j + 1 < ntiles) issue_s((j + 1) & 1);
-            }
+            warp_arrive(bar(kBarOFree + wg));
+            gt += it.nt;
         }
-        if (aborted) break;
-
-        // epilogue: O / l -> bf16 rows
-        if (ntiles > 0) {
-            if (!tc::mbar_wait(bar_pv, ph_pv)) { set_error(kErrTimeout); timed_out = 1; }
-            ph_pv ^= 1;
-            tc::fence_after_sync();
-        }
-        float lt = lsum;
-        const float inv = lt > 0.f ? 1.f / lt : 0.f;
-        uint4 *orow = reinterpret_cast<uint4 *>(outg + row_elem * kRowBytes);
+    } else if (warp == kKWarp || warp == kVWarp) {
+        // ---------------- K and V producers ----------------
+        // Per 64-key tile, lanes 0-7 each load one 16-key, 64-dim box (lane
+        // / 2: group, lane % 2: half) by TMA; a box at row -kGroup reads zeros
+        // (a bad block id reads as zeros the same way). The block ids of the
+        // next tile are read while this one is issued. V groups that hold the
+        // end of the keys are copied (rows past the end zeroed) by the warp.
+        const bool is_v = warp == kVWarp;
+        const int lane = tid & 31;
+        const int q = lane >> 1, h = lane & 1;
+        const void *map = is_v ? static_cast<const void *>(&tmap_v) : static_cast<const void *>(&tmap_k);
+        const uint32_t bar_full = bar(is_v ? kBarVFull : kBarKFull);
+        const uint32_t bar_empty = bar(is_v ? kBarVEmpty : kBarKEmpty);
+        uint32_t gt = 0;
+        bool ok = true;
 #pragma unroll 1
-        for (int ch = 0; ch < 4; ++ch) {
-            uint32_t o[32];
-            if (ntiles > 0) {
-                tc::tmem_ld32(tO + lane + ch * 32, o);
-                tc::tmem_ld_wait();
-            } else {
-#pragma unroll
-                for (int c = 0; c < 32; ++c) o[c] = 0u;
+        for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x) {
+            const Item it = make_item<G>(qp, n, L);
+            const int kend = kend_of(it);
+            // boxes this lane loads for tile j: K every group holding keys, V
+            // the groups wholly below kend
+            auto box_row = [&](int j) -> int {
+                const int k0 = j * kKeys;
+                const int ng = is_v ? groups_full(k0, kend) : groups_used(k0, kend);
+                if (lane >= 8 || j >= it.nt || q >= ng) return INT32_MIN;
+                const int64_t row = key_row(a, s, k0 + q * kGroup);
+                return row < 0 ? -kGroup : (int)row;
+            };
+            int row_next = box_row(0);
+#pragma unroll 1
+            for (int j = 0; j < it.nt; ++j) {
+                const int row = row_next;
+                row_next = box_row(j + 1);
+                const uint32_t gj = gt + j;
+                const int st = gj % kStages;
+                if (!warp_wait(bar_empty + 8 * st, ((gj / kStages) & 1) ^ 1, abort)) { ok = false; break; }
+                const uint32_t dst = sbase + kOffKV + st * 2 * kKVBytes + (is_v ? kKVBytes : 0);
+                const uint32_t full = bar_full + 8 * st;
+                const int k0 = j * kKeys;
+                const int nk = groups_used(k0, kend), nf = groups_full(k0, kend);
+                if (lane == 0) tc::mbar_expect_tx(full, (uint32_t)(is_v ? nf : nk) * 2 * kGroup * 128);
+                __syncwarp();
+                if (row != INT32_MIN)
+                    tc::tma_load_3d(dst + h * kKVHalf + q * kGroup * 128, map, h * 64, kvh, row, full);
+                if (is_v && nk > nf) {
+                    copy_v_tail(a, s, kvh, k0 + nf * kGroup, kend, dst, lane);
+                    tc::fence_proxy_async();
+                }
+                warp_arrive(full);
             }
-            if (rv) {
+            gt += it.nt;
+        }
+    } else if (warp == kQWarp) {
+        // ---------------- Q producer ----------------
+        const int lane = tid & 31;
+        const uint16_t *qg = static_cast<const uint16_t *>(a.q);
+        int item = 0;
+        bool ok = true;
+#pragma unroll 1
+        for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x, ++item) {
+            const Item it = make_item<G>(qp, n, L);
+            if (item > 0 && !warp_wait(bar(kBarQEmpty), (item - 1) & 1, abort)) { ok = false; break; }
+            // Q_A and Q_B: row r of the pair is token tok0 + r / G, head r % G
+#pragma unroll 8
+            for (int i = 0; i < (2 * kRows * 16) / 32; ++i) {
+                const int c = lane + i * 32;
+                const int row = c >> 4, chunk = c & 15;
+                const int tok = it.tok0 + row / G, head = row % G;
+                const bool rv = tok < n && head < g;
+                const int rr = row & (kRows - 1);
+                const uint32_t dst = sbase + kOffQ + (row >> 7) * kQBytes + (chunk >> 3) * kQHalf +
+                                     rr * 128 + ((((uint32_t)chunk & 7) ^ ((uint32_t)rr & 7)) << 4);
+                const int64_t e = ((int64_t)q0 + tok) * a.num_q_heads + (int64_t)kvh * g + head;
+                cp_async_16(dst, rv ? reinterpret_cast<const char *>(qg + e * kHeadDim) + chunk * 16
+                                    : static_cast<const void *>(qg),
+                            rv ? 16 : 0);
+            }
+            cp_async_commit();
+            cp_async_wait<0>();
+            tc::fence_proxy_async();
+            warp_arrive(bar(kBarQFull));
+        }
+    } else if (warp == kMmaWarp) {
+        // ---------------- MMA issue ----------------
+        // The whole warp runs the issue loop, converged, so that barrier
+        // tests and descriptors are warp-uniform; one elected lane executes
+        // each tcgen05.mma / commit.
+        // Descriptors: the high word (stride offset 1024 B, version, 128-byte
+        // swizzle) is common to all operands; the low word is (address >> 4)
+        // | leading offset, so a K step or another stage only adds a constant.
+        const uint32_t hi = (1024u >> 4) | (1u << 14) | (2u << 29);
+        const uint32_t lbo_k = 1u << 16;                        // K-major: 16 B (unused)
+        const uint32_t lbo_v = (kKVHalf >> 4) << 16;            // V: next 64 dims 8 KB on
+        const uint32_t q_lo = ((sbase + kOffQ) >> 4) | lbo_k;
+        const uint32_t p_lo = ((sbase + kOffP) >> 4) | lbo_k;
+        const uint32_t k_lo = ((sbase + kOffKV) >> 4) | lbo_k;
+        const uint32_t v_lo = ((sbase + kOffKV + kKVBytes) >> 4) | lbo_v;
+        auto desc = [hi](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
+        // S_t = Q_t K^T from K stage st
+        auto issue_s = [&](int t, int st, uint32_t release) {
+            const uint32_t q = q_lo + t * (kQBytes >> 4);
+            const uint32_t k = k_lo + st * (2 * kKVBytes >> 4);
+            const uint32_t d = tmem + t * kKeys;
+            tc::fence_after_sync();
+            if (tc::elect_one()) {
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {
-                    uint4 w;
-                    w.x = pack_bf16x2(__uint_as_float(o[8 * c + 0]) * inv, __uint_as_float(o[8 * c + 1]) * inv);
-                    w.y = pack_bf16x2(__uint_as_float(o[8 * c + 2]) * inv, __uint_as_float(o[8 * c + 3]) * inv);
-                    w.z = pack_bf16x2(__uint_as_float(o[8 * c + 4]) * inv, __uint_as_float(o[8 * c + 5]) * inv);
-                    w.w = pack_bf16x2(__uint_as_float(o[8 * c + 6]) * inv, __uint_as_float(o[8 * c + 7]) * inv);
-                    orow[ch * 4 + c] = w;
+                for (int kk = 0; kk < kHeadDim / 16; ++kk)
+                    tc::mma_ss(d, desc(q + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4)),
+                               desc(k + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4)), kIdescS, kk > 0);
+                tc::commit(bar(kBarSFull + t));
+                if (release) tc::commit(release);
+            }
+            __syncwarp();
+        };
+        // O_t += P_t V over the first nv 16-key groups of V stage st (the rest
+        // lie past the end of the keys: P is zero there and V is not loaded)
+        auto issue_pv = [&](int t, int st, bool acc, int nv, uint32_t release) {
+            const uint32_t p = p_lo + t * (kPBytes >> 4);
+            const uint32_t v = v_lo + st * (2 * kKVBytes >> 4);
+            const uint32_t d = tmem + 128 + t * 128;
+            tc::fence_after_sync();
+            if (tc::elect_one()) {
+#pragma unroll
+                for (int kk = 0; kk < kKeys / 16; ++kk)
+                    if (kk < nv)
+                        tc::mma_ss(d, desc(p + ((kk * 32) >> 4)), desc(v + ((kk * 2048) >> 4)), kIdescPV,
+                                   acc || kk > 0);
+                tc::commit(bar(kBarPVDone + t));
+                if (release) tc::commit(release);
+            }
+            __syncwarp();
+        };
+        auto ready = [](uint32_t b, uint32_t parity) {
+            return __shfl_sync(0xffffffffu, tc::mbar_test_wait(b, parity) ? 1 : 0, 0) != 0;
+        };
+        // Event-driven issue: whatever is ready, for either query tile: S_t(x)
+        // once K_x has landed and the softmax has read S_t(x - 1); PV_t(y)
+        // once P_t(y) is in shared memory and V_y has landed (and, for the
+        // first PV of an item, the previous item's O has been read). A K
+        // stage is released after the second S that reads it, a V stage
+        // after the second PV.
+        uint32_t gt = 0;
+        int item = 0;
+        bool ok = true;
+#pragma unroll 1
+        for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x, ++item) {
+            const Item it = make_item<G>(qp, n, L);
+            const int kend = kend_of(it);
+            ok = warp_wait(bar(kBarQFull), item & 1, abort);
+            int sj0 = 0, sj1 = 0, pj0 = 0, pj1 = 0;     // next S / PV tile of A, B
+            uint64_t t_idle = 0;
+            uint32_t idle = 0;
+#pragma unroll 1
+            while (ok && (pj0 < it.nt || pj1 < it.nt)) {
+                bool progress = false;
+#pragma unroll
+                for (int t = 0; t < 2; ++t) {
+                    int &sj = t == 0 ? sj0 : sj1;
+                    int &pj = t == 0 ? pj0 : pj1;
+                    const int other_pj = t == 0 ? pj1 : pj0;
+                    const int other_sj = t == 0 ? sj1 : sj0;
+                    if (sj < it.nt) {
+                        const uint32_t gs = gt + sj;
+                        const int st = gs % kStages;
+                        if (ready(bar(kBarKFull + st), (gs / kStages) & 1) &&
+                            (gs == 0 || ready(bar(kBarSFree + t), (gs - 1) & 1))) {
+                            issue_s(t, st, other_sj > sj ? bar(kBarKEmpty + st) : 0u);
+                            ++sj;
+                            progress = true;
+                        }
+                    }
+                    if (pj < sj) {
+                        const uint32_t gp = gt + pj;
+                        const int st = gp % kStages;
+                        bool go = ready(bar(kBarPReady + t), gp & 1) &&
+                                  ready(bar(kBarVFull + st), (gp / kStages) & 1);
+                        if (go && pj == 0 && item > 0) go = ready(bar(kBarOFree + t), (item - 1) & 1);
+                        if (go) {
+                            issue_pv(t, st, pj > 0, groups_used(pj * kKeys, kend),
+                                     other_pj > pj ? bar(kBarVEmpty + st) : 0u);
+                            ++pj;
+                            progress = true;
+                        }
+                    }
+                }
+                if (progress) {
+                    idle = 0;
+                    continue;
+                }
+                // nothing ready: back off briefly instead of polling the
+                // barrier words in a tight loop
+                __nanosleep(32);
+                if (++idle == 1) {
+                    t_idle = tc::globaltimer_ns();
+                } else if ((idle & 255) == 0) {
+                    const bool stop = __shfl_sync(0xffffffffu,
+                                                  (*abort || tc::globaltimer_ns() - t_idle > 2000000000ull) ? 1 : 0, 0) != 0;
+                    if (stop) {
+                        if ((threadIdx.x & 31) == 0 && !*abort) {
+                            set_error(kErrTimeout);
+                            *abort = 1;
+                        }
+                        ok = false;
+                    }
                 }
             }
+            // Q buffers free once this item's MMAs are done
+            if (tc::elect_one()) tc::commit(bar(kBarQEmpty));
+            __syncwarp();
+            gt += it.nt;
         }
-        cp_async_wait<0>();
-        tc::fence_before_sync();
-        // next tile rewrites Q, K/V, S and O
-        if (__syncthreads_or(timed_out)) aborted = true;
     }
 
-    cp_async_wait<0>();
+    // teardown: every role is done (or has given up); TMEM is freed
     tc::fence_before_sync();
     __syncthreads();
-    if (warp == 0) {
+    if (warp == kMmaWarp) {
         tc::fence_after_sync();
         tc::tmem_dealloc(tmem, kTmemCols);
     }
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void *p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// The pool [NB, bs, Hkv, 128] as a 3-D tensor (128, Hkv, NB * bs) of bf16 with
+// 16-token boxes of 64 dims of one head, 128-byte swizzle.
+bool make_pool_map(CUtensorMap *m, const void *pool, int64_t rows, int num_kv_heads) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_kv_heads, (cuuint64_t)rows};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)num_kv_heads * kRowBytes};
+    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kGroup};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
 template <int G>
@@ -347,10 +654,16 @@ cudaError_t launch_g(const PrefillArgs &a, int max_query_len, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
+    const int64_t rows = a.num_blocks << a.block_size_log2;
+    if (rows >= (int64_t)1 << 31) return cudaErrorInvalidValue;    // TMA row coordinates are int32
+    CUtensorMap mk, mv;
+    if (!make_pool_map(&mk, a.k_cache, rows, a.num_kv_heads) ||
+        !make_pool_map(&mv, a.v_cache, rows, a.num_kv_heads))
+        return cudaErrorInvalidValue;
     constexpr int BT = kRows / G;
-    int gx = (max_query_len + BT - 1) / BT;
+    int gx = (max_query_len + 2 * BT - 1) / (2 * BT);
     gx = gx < 1 ? 1 : (gx > 65535 ? 65535 : gx);
-    prefill_tc_kernel<G><<<dim3(gx, a.num_seqs, a.num_kv_heads), kThreads, kSmemBytes, st>>>(a);
+    prefill_tc_kernel<G><<<dim3(gx, a.num_seqs, a.num_kv_heads), kThreads, kSmemBytes, st>>>(a, mk, mv);
     return cudaGetLastError();
 }
 
