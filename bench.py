@@ -489,10 +489,17 @@ def prefill_oracle_sample(pb, target_s: float, host=None):
     return us, threads, sample
 
 
+def prefill_spec(args):
+    spec, chunk = inputs.PREFILL_SPECS[args.workload]
+    if args.num_seqs:
+        spec = inputs.scaled(spec, num_seqs=args.num_seqs, name=f"{spec.name}_s{args.num_seqs}")
+    return spec, chunk
+
+
 def run_reference_prefill(args, rank, world):
     if rank != 0:
         return
-    spec, chunk = inputs.PREFILL_SPECS[args.workload]
+    spec, chunk = prefill_spec(args)
     pb = inputs.prefill_batch(spec, seed=0, chunk=chunk)
     per_step = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
     for _ in range(args.warmup):
@@ -517,7 +524,7 @@ def run_gpu_prefill(args, rank, world, local):
     from paged_kv_cache_255_gb300 import pagedattn as pa
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
-    spec, chunk = inputs.PREFILL_SPECS[args.workload]
+    spec, chunk = prefill_spec(args)
     pb = inputs.prefill_batch(spec, seed=0, chunk=chunk)
     wl = pb.wl
     k_cache, v_cache = wl.k_cache.to(dev), wl.v_cache.to(dev)
