@@ -2,45 +2,50 @@
 // attention as prefill.cu (chunk rows of a sequence attend causally to its
 // tokens in the paged KV cache; "A vLLM engine small enough to read in one
 // sitting": prefill and decode run over the paged KV cache, flash attention
-// for prefill), computed in the flash-attention order with the two
-// contractions on tcgen05.mma and all accumulators in tensor memory.
+// for prefill), computed in the flash-attention order with both contractions
+// on tcgen05.mma, S, P and O in tensor memory.
 //
 // One CTA per SM owns two 128-row query tiles A and B of one (sequence, KV
 // head); a tile is 128 / G query tokens x the G query heads of the group (G =
 // group size rounded up to a power of two), so every K/V tile fetched serves
-// 256 rows. Warp roles:
+// 256 rows. Keys go in tiles of 128. TMEM (512 columns): S_A 0-127, O_A
+// 128-255, S_B 256-383, O_B 384-511; P_t (bf16, two per column) overwrites
+// the first 64 columns of S_t. Warp roles:
 //   warps 0-3, 4-7   softmax of tile A, B: thread t of the warpgroup owns row
-//                    t, which is TMEM lane t. Per 64-key tile j it reads its
-//                    row of S_j (tcgen05.ld), masks it causally, updates its
-//                    running max and sum, writes P_j (bf16) to shared memory.
-//   warps 8, 9       K and V producers: per 64-key tile, 8 lanes each fetch
-//                    16-token boxes of one KV head by TMA through a 3-D tensor
-//                    map over the pool ([NB * bs, Hkv, 128]), landing in the
-//                    128-byte swizzled layout the MMA descriptors name, into
-//                    4-stage rings. A K stage is refilled as soon as both S
-//                    of its tile are done, a V stage after both PV. V rows of
-//                    a partly used 16-token group at the end of the keys are
-//                    copied (and the rows past the end zeroed) by the lanes.
+//                    t (TMEM lane t). Per key tile j it reads its row of S_j
+//                    (tcgen05.ld, two passes: the max, then P), masks it
+//                    causally on the tiles that reach its limit, keeps a
+//                    running max (raised only when a tile's max exceeds it by
+//                    more than 2^8 in exp2 units; then it rescales its row of
+//                    O in TMEM) and sum, and writes P_j (tcgen05.st).
+//   warps 8, 9       K and V producers: per tile, 16 lanes each fetch one
+//                    box of 16 tokens x 64 dims of one KV head by TMA through
+//                    a 3-D tensor map over the pool ([NB * bs, Hkv, 128]),
+//                    landing in the 128-byte swizzled layout the MMA
+//                    descriptors name, into 3 K stages and 2 V stages. V rows
+//                    of a partly used 16-token group at the end of the keys
+//                    are copied (rows past the end zeroed) by the lanes.
 //   warp 10          Q producer: both query tiles, by 16-byte cp.async.
-//   warp 11          issues the MMAs (one elected lane), S_t(j) = Q_t K_j^T and
-//                    O_t += P_t(j) V_j for t in {A, B}, each as soon as its
-//                    inputs are ready (S_t(j + 1) is computed while the
-//                    softmax works on S_t(j)); 16-token groups of V wholly
-//                    past the end of the keys are left out of PV.
-// The running max is raised only when a tile's max exceeds it by more than
-// 2^8 (in exp2 units); otherwise the stale max is kept, which changes nothing
-// in O / l but the rounding. When it is raised, the warp rescales its rows of
-// O in TMEM before the next PV.
+//   warp 11          issues the MMAs (converged warp, one elected lane):
+//                      S_t(j)  = Q_t K_j^T      M 128, N 128, K 16 x 8 (smem, smem)
+//                      O_t    += P_t(j) V_j     M 128, N 128, K 16 x 8 (TMEM, smem)
+//                    as soon as their inputs are ready; S_t(j + 1) follows
+//                    PV_t(j) in issue order, so the tensor core has read P_t(j)
+//                    before S_t(j + 1) overwrites it, and a softmax warp that
+//                    sees S_t(j + 1) knows PV_t(j) has finished (O is stable).
+//                    16-token V groups wholly past the end of the keys are
+//                    left out of PV.
 //
 // Hand-offs are mbarriers: k_full / v_full complete when the TMA bytes have
 // landed and the producer warp has arrived (after fencing its own
-// shared-memory writes to the async proxy); q_full when the Q warp's copies have landed and been
-// fenced; tcgen05.commit arrives on
-// s_full, pv_done, k_empty and v_empty; the softmax threads arrive on s_free once
-// their row of S is in registers and on p_ready once P is in shared memory
-// (and O rescaled). Every wait is bounded (about 2 s) and also gives up once
-// any thread of the CTA has recorded a failed wait; then every role skips to
-// the end, where the CTA frees its TMEM and exits.
+// shared-memory writes to the async proxy); q_full when the Q warp's copies
+// have landed and been fenced; tcgen05.commit arrives on s_full, pv_done,
+// k_empty and v_empty; the softmax warps arrive on p_ready once P is in TMEM
+// (and O rescaled), and on o_free once the epilogue has read O. Every wait is
+// bounded (about 2 s) and also gives up once any thread of the CTA has
+// recorded a failed wait; then every role skips to the end, where the CTA
+// frees its TMEM and exits.
+#include <climits>
 #include <cmath>
 #include <mutex>
 
@@ -58,8 +63,9 @@ __device__ int g_prefill_error;      // first device-side error of a prefill lau
 namespace {
 
 constexpr int kRows = 128;                              // rows per query tile
-constexpr int kKeys = 64;                               // keys per K/V tile
-constexpr int kStages = 4;
+constexpr int kKeys = 128;                              // keys per K/V tile
+constexpr int kKStages = 3;
+constexpr int kVStages = 2;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kKWarp = kSoftmaxThreads / 32;             // 8
 constexpr int kVWarp = kKWarp + 1;                       // 9
@@ -67,25 +73,24 @@ constexpr int kQWarp = kKWarp + 2;                       // 10
 constexpr int kMmaWarp = kKWarp + 3;                     // 11
 constexpr int kThreads = kSoftmaxThreads + 4 * 32;
 constexpr int kGroup = 16;                               // tokens per TMA box
+constexpr int kGroups = kKeys / kGroup;                  // 8
 constexpr uint32_t kQBytes = kRows * kRowBytes;         // 32 KB: 2 K-halves of [128][128 B]
 constexpr uint32_t kQHalf = kRows * 128;                // 16 KB
-constexpr uint32_t kKVBytes = kKeys * kRowBytes;        // 16 KB: 2 halves of [64][128 B]
-constexpr uint32_t kKVHalf = kKeys * 128;               // 8 KB
-constexpr uint32_t kPBytes = kRows * kKeys * 2;         // 16 KB: [128][128 B]
+constexpr uint32_t kKVBytes = kKeys * kRowBytes;        // 32 KB: 2 halves of [128][128 B]
+constexpr uint32_t kKVHalf = kKeys * 128;               // 16 KB
 constexpr uint32_t kOffQ = 0;                           // Q_A, Q_B
-constexpr uint32_t kOffP = kOffQ + 2 * kQBytes;         // P_A, P_B
-constexpr uint32_t kOffKV = kOffP + 2 * kPBytes;        // stage i: K at i * 32 KB, V 16 KB on
-constexpr uint32_t kOffCtl = kOffKV + kStages * 2 * kKVBytes;
+constexpr uint32_t kOffK = kOffQ + 2 * kQBytes;         // K stages
+constexpr uint32_t kOffV = kOffK + kKStages * kKVBytes; // V stages
+constexpr uint32_t kOffCtl = kOffV + kVStages * kKVBytes;
 // control block: mbarriers (8 B each), then the TMEM base and the abort flag
 constexpr uint32_t kBarQFull = 0;
 constexpr uint32_t kBarQEmpty = 1;
-constexpr uint32_t kBarKFull = 2;                       // + stage
-constexpr uint32_t kBarKEmpty = kBarKFull + kStages;    // + stage
-constexpr uint32_t kBarVFull = kBarKEmpty + kStages;    // + stage
-constexpr uint32_t kBarVEmpty = kBarVFull + kStages;    // + stage
-constexpr uint32_t kBarSFull = kBarVEmpty + kStages;    // + tile (A 0, B 1)
-constexpr uint32_t kBarSFree = kBarSFull + 2;
-constexpr uint32_t kBarPReady = kBarSFree + 2;
+constexpr uint32_t kBarKFull = 2;                        // + stage
+constexpr uint32_t kBarKEmpty = kBarKFull + kKStages;    // + stage
+constexpr uint32_t kBarVFull = kBarKEmpty + kKStages;    // + stage
+constexpr uint32_t kBarVEmpty = kBarVFull + kVStages;    // + stage
+constexpr uint32_t kBarSFull = kBarVEmpty + kVStages;    // + query tile (A 0, B 1)
+constexpr uint32_t kBarPReady = kBarSFull + 2;
 constexpr uint32_t kBarPVDone = kBarPReady + 2;
 constexpr uint32_t kBarOFree = kBarPVDone + 2;
 constexpr uint32_t kNumBars = kBarOFree + 2;
@@ -93,7 +98,7 @@ constexpr uint32_t kOffTmemSlot = kOffCtl + 8 * kNumBars;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
 constexpr uint32_t kSmemBytes = kOffCtl + 256;
 static_assert(kOffAbort + 4 <= kSmemBytes, "control block");
-// TMEM: S_A 0-63, S_B 64-127, O_A 128-255, O_B 256-383
+static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, kKeys, false);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, true);
@@ -107,9 +112,7 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
 
-// Bounded wait that also gives up once the CTA's abort flag is set. Between
-// checks the thread sleeps in the barrier (woken when the phase completes), so
-// that waiting warps leave shared-memory bandwidth to the tensor core.
+// Bounded wait that also gives up once the CTA's abort flag is set.
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int *abort) {
     if (tc::mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = tc::globaltimer_ns();
@@ -125,8 +128,7 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // Warp-level hand-offs: one lane waits (or arrives) for the whole warp, the
-// others are ordered with it by __syncwarp. Fewer arrivals and polls on the
-// barrier words leave shared memory to the tensor core's operand reads.
+// others are ordered with it by __syncwarp.
 __device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
     bool ok = true;
     if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort);
@@ -177,18 +179,19 @@ __device__ __forceinline__ void copy_v_tail(const PrefillArgs &a, int s, int kvh
 // those wholly below kend.
 __device__ __forceinline__ int groups_used(int k0, int kend) {
     const int n = (kend - k0 + kGroup - 1) / kGroup;
-    return n < 0 ? 0 : (n > kKeys / kGroup ? kKeys / kGroup : n);
+    return n < 0 ? 0 : (n > kGroups ? kGroups : n);
 }
 __device__ __forceinline__ int groups_full(int k0, int kend) {
     const int n = (kend - k0) / kGroup;
-    return n < 0 ? 0 : (n > kKeys / kGroup ? kKeys / kGroup : n);
+    return n < 0 ? 0 : (n > kGroups ? kGroups : n);
 }
 
 // Work item: a pair of query tiles (2 x 128 / G tokens) of one (sequence, KV
 // head). Every role walks the same items and computes the same bounds.
 struct Item {
     int tok0;       // first token of tile A
-    int nt;         // K/V tiles the pair reads
+    int kend;       // keys the pair reads: L - n + (its last token) + 1
+    int nt;         // K/V tiles
 };
 
 template <int G>
@@ -198,8 +201,8 @@ __device__ __forceinline__ Item make_item(int qp, int n, int L) {
     it.tok0 = qp * 2 * BT;
     const int last_tok = (it.tok0 + 2 * BT < n ? it.tok0 + 2 * BT : n) - 1;
     int kend = L - n + last_tok + 1;
-    kend = kend < 0 ? 0 : (kend > L ? L : kend);
-    it.nt = (kend + kKeys - 1) / kKeys;
+    it.kend = kend < 0 ? 0 : (kend > L ? L : kend);
+    it.nt = (it.kend + kKeys - 1) / kKeys;
     return it;
 }
 
@@ -233,12 +236,6 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         const int64_t max_len = (int64_t)a.max_blocks_per_seq << a.block_size_log2;
         L = L < 0 ? 0 : ((int64_t)L > max_len ? (int)max_len : L);
     }
-    // kend of a pair: L - n + (its last token) + 1
-    auto kend_of = [&](const Item &it) {
-        const int last_tok = (it.tok0 + 2 * BT < n ? it.tok0 + 2 * BT : n) - 1;
-        const int k = L - n + last_tok + 1;
-        return k < 0 ? 0 : (k > L ? L : k);
-    };
 
     const uint32_t ctl = sbase + kOffCtl;
     auto bar = [&](uint32_t i) { return ctl + 8 * i; };
@@ -246,15 +243,16 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
     if (tid == 0) {
         tc::mbar_init(bar(kBarQFull), 1);
         tc::mbar_init(bar(kBarQEmpty), 1);
-        for (int i = 0; i < kStages; ++i) {
+        for (int i = 0; i < kKStages; ++i) {
             tc::mbar_init(bar(kBarKFull + i), 1);
             tc::mbar_init(bar(kBarKEmpty + i), 1);
+        }
+        for (int i = 0; i < kVStages; ++i) {
             tc::mbar_init(bar(kBarVFull + i), 1);
             tc::mbar_init(bar(kBarVEmpty + i), 1);
         }
         for (int i = 0; i < 2; ++i) {
             tc::mbar_init(bar(kBarSFull + i), 1);
-            tc::mbar_init(bar(kBarSFree + i), kRows / 32);
             tc::mbar_init(bar(kBarPReady + i), kRows / 32);
             tc::mbar_init(bar(kBarPVDone + i), 1);
             tc::mbar_init(bar(kBarOFree + i), kRows / 32);
@@ -272,9 +270,11 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         // ---------------- softmax warpgroups ----------------
         const int wg = tid >> 7, r = tid & 127;
         const uint32_t lane = (uint32_t)(r & ~31) << 16;
-        const uint32_t tS = tmem + wg * kKeys, tO = tmem + 128 + wg * 128;
-        const uint32_t sP = sbase + kOffP + wg * kPBytes;
+        const uint32_t tS = tmem + lane + wg * 256, tO = tS + 128;
         const float sc = a.scale_log2;
+        // a masked score for the max: the value that loses whatever the
+        // scale's sign (masked keys then get p = 0 directly)
+        const float masked = sc >= 0.f ? -INFINITY : INFINITY;
         uint32_t gt = 0;                        // tiles done before this item
         bool ok = true;
 #pragma unroll 1
@@ -291,28 +291,29 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
 #pragma unroll 1
             for (int j = 0; j < it.nt; ++j) {
                 const uint32_t gj = gt + j;
+                // S_t(j) done: also PV_t(j - 1) (issued before it), so O is stable
                 if (!warp_wait(bar(kBarSFull + wg), gj & 1, abort)) { ok = false; break; }
                 tc::fence_after_sync();
-                uint32_t sr[2][32];
-                tc::tmem_ld32(tS + lane, sr[0]);
-                tc::tmem_ld32(tS + lane + 32, sr[1]);
-                tc::tmem_ld_wait();
-                tc::fence_before_sync();
-                warp_arrive(bar(kBarSFree + wg));
-
-                // scores in exp2 units, causal mask, lazily raised max,
-                // P = 2^(S sc - m)
                 const int kb = j * kKeys;
-                float mt = -INFINITY;
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
+                const bool need_mask = kb + kKeys > lim;
+                // pass 1: the tile's max of the scores (raw, then scaled)
+                float mx = -INFINITY, mn = INFINITY;
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t sr[32];
+                    tc::tmem_ld32(tS + ch * 32, sr);
+                    tc::tmem_ld_wait();
 #pragma unroll
                     for (int c = 0; c < 32; ++c) {
-                        float v = __uint_as_float(sr[h][c]) * sc;
-                        if (kb + h * 32 + c >= lim) v = -INFINITY;
-                        sr[h][c] = __float_as_uint(v);
-                        mt = fmaxf(mt, v);
+                        float v = __uint_as_float(sr[c]);
+                        if (need_mask && kb + ch * 32 + c >= lim) v = masked;
+                        mx = fmaxf(mx, v);
+                        mn = fminf(mn, v);
                     }
+                }
+                // every score of the row masked: no new max (also for scale 0)
+                const float ext = sc >= 0.f ? mx : mn;
+                const float mt = ext == masked ? -INFINITY : ext * sc;
                 bool rescale = false;
                 float alpha = 1.f;
                 if (mt > m + kRescaleSlack) {
@@ -322,45 +323,40 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                     m = mt;
                 }
                 const float mb = m == -INFINITY ? 0.f : m;
-                uint32_t pw[32];
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
+                // pass 2: P = 2^(S sc - m) in bf16 over the first 64 columns
+                // (chunk ch of S -> columns 16 ch .. 16 ch + 15: already read)
+#pragma unroll 1
+                for (int ch = 0; ch < 4; ++ch) {
+                    uint32_t sr[32];
+                    tc::tmem_ld32(tS + ch * 32, sr);
+                    tc::tmem_ld_wait();
+                    uint32_t pw[16];
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const float p0 = ex2(__uint_as_float(sr[h][2 * c]) - mb);
-                        const float p1 = ex2(__uint_as_float(sr[h][2 * c + 1]) - mb);
-                        const uint32_t w = pack_bf16x2(p0, p1);
-                        lsum += bf16_lo(w) + bf16_hi(w);
-                        pw[h * 16 + c] = w;
+                        const int k = kb + ch * 32 + 2 * c;
+                        float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sc, -mb));
+                        float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sc, -mb));
+                        if (need_mask && k >= lim) p0 = 0.f;
+                        if (need_mask && k + 1 >= lim) p1 = 0.f;
+                        lsum += p0 + p1;
+                        pw[c] = pack_bf16x2(p0, p1);
                     }
-
-                // PV(j-1) done: O stable, P buffer free
-                if (j > 0) {
-                    if (!warp_wait(bar(kBarPVDone + wg), (gj - 1) & 1, abort)) { ok = false; break; }
-                    tc::fence_after_sync();
+                    tc::tmem_st16(tS + ch * 16, pw);
                 }
+                // rescale this warp's rows of O if any of them raised its max
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
                     for (int ch = 0; ch < 4; ++ch) {
                         uint32_t o[32];
-                        tc::tmem_ld32(tO + lane + ch * 32, o);
+                        tc::tmem_ld32(tO + ch * 32, o);
                         tc::tmem_ld_wait();
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
                             o[c] = __float_as_uint(__uint_as_float(o[c]) * alpha);
-                        tc::tmem_st32(tO + lane + ch * 32, o);
+                        tc::tmem_st32(tO + ch * 32, o);
                     }
-                    tc::tmem_st_wait();
                 }
-#pragma unroll
-                for (int c = 0; c < 8; ++c) {
-                    const uint32_t dst = sP + r * 128 + ((((uint32_t)c) ^ ((uint32_t)r & 7)) << 4);
-                    asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};\n" ::"r"(dst),
-                                 "r"(pw[4 * c]), "r"(pw[4 * c + 1]), "r"(pw[4 * c + 2]),
-                                 "r"(pw[4 * c + 3])
-                                 : "memory");
-                }
-                tc::fence_proxy_async();
+                tc::tmem_st_wait();
                 tc::fence_before_sync();
                 warp_arrive(bar(kBarPReady + wg));
             }
@@ -377,7 +373,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t o[32];
                 if (it.nt > 0) {
-                    tc::tmem_ld32(tO + lane + ch * 32, o);
+                    tc::tmem_ld32(tO + ch * 32, o);
                     tc::tmem_ld_wait();
                 } else {
 #pragma unroll
@@ -401,29 +397,29 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         }
     } else if (warp == kKWarp || warp == kVWarp) {
         // ---------------- K and V producers ----------------
-        // Per 64-key tile, lanes 0-7 each load one 16-key, 64-dim box (lane
-        // / 2: group, lane % 2: half) by TMA; a box at row -kGroup reads zeros
-        // (a bad block id reads as zeros the same way). The block ids of the
-        // next tile are read while this one is issued. V groups that hold the
-        // end of the keys are copied (rows past the end zeroed) by the warp.
+        // Per key tile, lane i < 16 loads the box of 16-key group i / 2, half
+        // i % 2 by TMA; a box at row -kGroup reads zeros (a bad block id reads
+        // as zeros the same way). The block ids of the next tile are read
+        // while this one is issued. The V group holding the end of the keys
+        // is copied by the warp with the rows past the end zeroed.
         const bool is_v = warp == kVWarp;
+        const int nst = is_v ? kVStages : kKStages;
         const int lane = tid & 31;
         const int q = lane >> 1, h = lane & 1;
         const void *map = is_v ? static_cast<const void *>(&tmap_v) : static_cast<const void *>(&tmap_k);
         const uint32_t bar_full = bar(is_v ? kBarVFull : kBarKFull);
         const uint32_t bar_empty = bar(is_v ? kBarVEmpty : kBarKEmpty);
+        const uint32_t base = sbase + (is_v ? kOffV : kOffK);
         uint32_t gt = 0;
         bool ok = true;
 #pragma unroll 1
         for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x) {
             const Item it = make_item<G>(qp, n, L);
-            const int kend = kend_of(it);
-            // boxes this lane loads for tile j: K every group holding keys, V
-            // the groups wholly below kend
+            const int kend = it.kend;
             auto box_row = [&](int j) -> int {
                 const int k0 = j * kKeys;
                 const int ng = is_v ? groups_full(k0, kend) : groups_used(k0, kend);
-                if (lane >= 8 || j >= it.nt || q >= ng) return INT32_MIN;
+                if (lane >= 2 * kGroups || j >= it.nt || q >= ng) return INT_MIN;
                 const int64_t row = key_row(a, s, k0 + q * kGroup);
                 return row < 0 ? -kGroup : (int)row;
             };
@@ -433,15 +429,15 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 const int row = row_next;
                 row_next = box_row(j + 1);
                 const uint32_t gj = gt + j;
-                const int st = gj % kStages;
-                if (!warp_wait(bar_empty + 8 * st, ((gj / kStages) & 1) ^ 1, abort)) { ok = false; break; }
-                const uint32_t dst = sbase + kOffKV + st * 2 * kKVBytes + (is_v ? kKVBytes : 0);
+                const int st = gj % nst;
+                if (!warp_wait(bar_empty + 8 * st, ((gj / nst) & 1) ^ 1, abort)) { ok = false; break; }
+                const uint32_t dst = base + st * kKVBytes;
                 const uint32_t full = bar_full + 8 * st;
                 const int k0 = j * kKeys;
                 const int nk = groups_used(k0, kend), nf = groups_full(k0, kend);
                 if (lane == 0) tc::mbar_expect_tx(full, (uint32_t)(is_v ? nf : nk) * 2 * kGroup * 128);
                 __syncwarp();
-                if (row != INT32_MIN)
+                if (row != INT_MIN)
                     tc::tma_load_3d(dst + h * kKVHalf + q * kGroup * 128, map, h * 64, kvh, row, full);
                 if (is_v && nk > nf) {
                     copy_v_tail(a, s, kvh, k0 + nf * kGroup, kend, dst, lane);
@@ -485,47 +481,45 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         // ---------------- MMA issue ----------------
         // The whole warp runs the issue loop, converged, so that barrier
         // tests and descriptors are warp-uniform; one elected lane executes
-        // each tcgen05.mma / commit.
-        // Descriptors: the high word (stride offset 1024 B, version, 128-byte
-        // swizzle) is common to all operands; the low word is (address >> 4)
-        // | leading offset, so a K step or another stage only adds a constant.
+        // each tcgen05.mma / commit. Descriptor high word (stride offset
+        // 1024 B, version, 128-byte swizzle) is common; the low word is
+        // (address >> 4) | leading offset.
         const uint32_t hi = (1024u >> 4) | (1u << 14) | (2u << 29);
         const uint32_t lbo_k = 1u << 16;                        // K-major: 16 B (unused)
-        const uint32_t lbo_v = (kKVHalf >> 4) << 16;            // V: next 64 dims 8 KB on
+        const uint32_t lbo_v = (kKVHalf >> 4) << 16;            // V: next 64 dims 16 KB on
         const uint32_t q_lo = ((sbase + kOffQ) >> 4) | lbo_k;
-        const uint32_t p_lo = ((sbase + kOffP) >> 4) | lbo_k;
-        const uint32_t k_lo = ((sbase + kOffKV) >> 4) | lbo_k;
-        const uint32_t v_lo = ((sbase + kOffKV + kKVBytes) >> 4) | lbo_v;
+        const uint32_t k_lo = ((sbase + kOffK) >> 4) | lbo_k;
+        const uint32_t v_lo = ((sbase + kOffV) >> 4) | lbo_v;
         auto desc = [hi](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
         // S_t = Q_t K^T from K stage st
         auto issue_s = [&](int t, int st, uint32_t release) {
-            const uint32_t q = q_lo + t * (kQBytes >> 4);
-            const uint32_t k = k_lo + st * (2 * kKVBytes >> 4);
-            const uint32_t d = tmem + t * kKeys;
+            const uint32_t qd = q_lo + t * (kQBytes >> 4);
+            const uint32_t kd = k_lo + st * (kKVBytes >> 4);
+            const uint32_t d = tmem + t * 256;
             tc::fence_after_sync();
             if (tc::elect_one()) {
 #pragma unroll
                 for (int kk = 0; kk < kHeadDim / 16; ++kk)
-                    tc::mma_ss(d, desc(q + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4)),
-                               desc(k + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4)), kIdescS, kk > 0);
+                    tc::mma_ss(d, desc(qd + (((kk >> 2) * kQHalf + (kk & 3) * 32) >> 4)),
+                               desc(kd + (((kk >> 2) * kKVHalf + (kk & 3) * 32) >> 4)), kIdescS, kk > 0);
                 tc::commit(bar(kBarSFull + t));
                 if (release) tc::commit(release);
             }
             __syncwarp();
         };
-        // O_t += P_t V over the first nv 16-key groups of V stage st (the rest
-        // lie past the end of the keys: P is zero there and V is not loaded)
+        // O_t += P_t V over the first nv 16-key groups of V stage st (P_t in
+        // TMEM, 8 columns per 16 keys; the groups past the end of the keys
+        // have P = 0 and no V)
         auto issue_pv = [&](int t, int st, bool acc, int nv, uint32_t release) {
-            const uint32_t p = p_lo + t * (kPBytes >> 4);
-            const uint32_t v = v_lo + st * (2 * kKVBytes >> 4);
-            const uint32_t d = tmem + 128 + t * 128;
+            const uint32_t vd = v_lo + st * (kKVBytes >> 4);
+            const uint32_t pa_ = tmem + t * 256;
+            const uint32_t d = pa_ + 128;
             tc::fence_after_sync();
             if (tc::elect_one()) {
 #pragma unroll
-                for (int kk = 0; kk < kKeys / 16; ++kk)
+                for (int kk = 0; kk < kGroups; ++kk)
                     if (kk < nv)
-                        tc::mma_ss(d, desc(p + ((kk * 32) >> 4)), desc(v + ((kk * 2048) >> 4)), kIdescPV,
-                                   acc || kk > 0);
+                        tc::mma_ts(d, pa_ + kk * 8, desc(vd + ((kk * 2048) >> 4)), kIdescPV, acc || kk > 0);
                 tc::commit(bar(kBarPVDone + t));
                 if (release) tc::commit(release);
             }
@@ -534,19 +528,17 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         auto ready = [](uint32_t b, uint32_t parity) {
             return __shfl_sync(0xffffffffu, tc::mbar_test_wait(b, parity) ? 1 : 0, 0) != 0;
         };
-        // Event-driven issue: whatever is ready, for either query tile: S_t(x)
-        // once K_x has landed and the softmax has read S_t(x - 1); PV_t(y)
-        // once P_t(y) is in shared memory and V_y has landed (and, for the
-        // first PV of an item, the previous item's O has been read). A K
-        // stage is released after the second S that reads it, a V stage
-        // after the second PV.
+        // Event-driven issue for each query tile t: S_t(x) once K_x has
+        // landed and PV_t(x - 1) has been issued; PV_t(y) once P_t(y) is in
+        // TMEM and V_y has landed (and, for the first PV of an item, the
+        // previous item's O has been read). A K stage is released after the
+        // second S that reads it, a V stage after the second PV.
         uint32_t gt = 0;
         int item = 0;
         bool ok = true;
 #pragma unroll 1
         for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x, ++item) {
             const Item it = make_item<G>(qp, n, L);
-            const int kend = kend_of(it);
             ok = warp_wait(bar(kBarQFull), item & 1, abort);
             int sj0 = 0, sj1 = 0, pj0 = 0, pj1 = 0;     // next S / PV tile of A, B
             uint64_t t_idle = 0;
@@ -560,26 +552,25 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                     int &pj = t == 0 ? pj0 : pj1;
                     const int other_pj = t == 0 ? pj1 : pj0;
                     const int other_sj = t == 0 ? sj1 : sj0;
-                    if (sj < it.nt) {
-                        const uint32_t gs = gt + sj;
-                        const int st = gs % kStages;
-                        if (ready(bar(kBarKFull + st), (gs / kStages) & 1) &&
-                            (gs == 0 || ready(bar(kBarSFree + t), (gs - 1) & 1))) {
-                            issue_s(t, st, other_sj > sj ? bar(kBarKEmpty + st) : 0u);
-                            ++sj;
+                    if (pj < sj) {
+                        const uint32_t gp = gt + pj;
+                        const int st = gp % kVStages;
+                        bool go = ready(bar(kBarPReady + t), gp & 1) &&
+                                  ready(bar(kBarVFull + st), (gp / kVStages) & 1);
+                        if (go && pj == 0 && item > 0) go = ready(bar(kBarOFree + t), (item - 1) & 1);
+                        if (go) {
+                            issue_pv(t, st, pj > 0, groups_used(pj * kKeys, it.kend),
+                                     other_pj > pj ? bar(kBarVEmpty + st) : 0u);
+                            ++pj;
                             progress = true;
                         }
                     }
-                    if (pj < sj) {
-                        const uint32_t gp = gt + pj;
-                        const int st = gp % kStages;
-                        bool go = ready(bar(kBarPReady + t), gp & 1) &&
-                                  ready(bar(kBarVFull + st), (gp / kStages) & 1);
-                        if (go && pj == 0 && item > 0) go = ready(bar(kBarOFree + t), (item - 1) & 1);
-                        if (go) {
-                            issue_pv(t, st, pj > 0, groups_used(pj * kKeys, kend),
-                                     other_pj > pj ? bar(kBarVEmpty + st) : 0u);
-                            ++pj;
+                    if (sj == pj && sj < it.nt) {
+                        const uint32_t gs = gt + sj;
+                        const int st = gs % kKStages;
+                        if (ready(bar(kBarKFull + st), (gs / kKStages) & 1)) {
+                            issue_s(t, st, other_sj > sj ? bar(kBarKEmpty + st) : 0u);
+                            ++sj;
                             progress = true;
                         }
                     }
@@ -588,8 +579,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                     idle = 0;
                     continue;
                 }
-                // nothing ready: back off briefly instead of polling the
-                // barrier words in a tight loop
+                // nothing ready: back off briefly
                 __nanosleep(32);
                 if (++idle == 1) {
                     t_idle = tc::globaltimer_ns();

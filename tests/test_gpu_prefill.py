@@ -143,19 +143,23 @@ def _sampled_rows_ref(pb, kc, vc, rows):
 
 
 @pytest.mark.parametrize("kernel", KERNELS)
-def test_negative_scale(kernel, monkeypatch):
+@pytest.mark.parametrize("scale", [-0.3, 0.0])
+def test_negative_and_zero_scale(kernel, scale, monkeypatch):
+    """A negative scale flips which score is the max; scale 0 is uniform
+    attention over the visible keys (masked keys still get nothing)."""
     monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
     spec = _spec("k", 16, 8, 16)
-    pb = inputs.prefill_batch(spec, seed=66, context_lens=[150, 40], chunk_lens=[100, 40])
+    pb = inputs.prefill_batch(spec, seed=66, context_lens=[150, 40, 300],
+                              chunk_lens=[100, 40, 260])
     kc, vc = _oracle_caches(pb)
     ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
-                               pb.query_start_loc, -0.3)
+                               pb.query_start_loc, scale)
     d = _device(pb)
     pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
     out = pa.prefill(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
-                     d["qsl"], -0.3)
+                     d["qsl"], scale)
     torch.cuda.synchronize()
-    gu.assert_close(out, ref, f"negative scale ({kernel})")
+    gu.assert_close(out, ref, f"scale {scale} ({kernel})")
 
 
 @pytest.mark.parametrize("name", sorted(PS))
