@@ -99,6 +99,22 @@ class ClockSampler:
         except (OSError, FileNotFoundError):
             self.proc = None
 
+    def wait_first_sample(self, timeout_s: float = 5.0):
+        """nvidia-smi's start-up can stall the GPU for a moment: start the
+        sampler before the warm-up and wait for its first line, so that the
+        start never falls in a timed region."""
+        if self.proc is None:
+            return
+        t0 = time.time()
+        while time.time() - t0 < timeout_s:
+            self.fh.flush()
+            try:
+                if os.path.getsize(self.path) > 0:
+                    return
+            except OSError:
+                return
+            time.sleep(0.05)
+
     def stop(self):
         if self.proc is None:
             return None
@@ -283,11 +299,12 @@ def run_gpu(args, rank, world, local):
 
     # ---- device-resident timing: store then decode back to back, as a user
     # issues them (the decode launch may overlap the store's tail)
+    clocks = ClockSampler(local)
+    clocks.wait_first_sample()
     for _ in range(args.warmup):
         flush.zero_()
         step()
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()
@@ -541,11 +558,12 @@ def run_gpu_prefill(args, rank, world, local):
         pa.store_kvcache(kn_, vn_, k_cache, v_cache, sl_)
         pa.prefill(q_, k_cache, v_cache, bt_, cl_, qsl_, wl.scale, max_query_len=mql, out=out)
 
+    clocks = ClockSampler(local)
+    clocks.wait_first_sample()
     for _ in range(args.warmup):
         flush.zero_()
         step(q, k_new, v_new, slots, bt, cl, qsl)
     torch.cuda.synchronize()
-    clocks = ClockSampler(local)
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
     barrier(world)
     torch.cuda.synchronize()

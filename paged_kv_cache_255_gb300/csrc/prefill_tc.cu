@@ -108,6 +108,18 @@ enum : int { kErrSmemAlign = 1, kErrTimeout = 2 };
 
 __device__ __forceinline__ void set_error(int code) { atomicCAS(&g_prefill_error, 0, code); }
 
+// Three-input max / min (one instruction on sm_100-family parts).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float r;
+    asm("max.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+__device__ __forceinline__ float fmin3(float a, float b, float c) {
+    float r;
+    asm("min.f32 %0, %1, %2, %3;\n" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+    return r;
+}
+
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
 }
@@ -296,23 +308,41 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 tc::fence_after_sync();
                 const int kb = j * kKeys;
                 const bool need_mask = kb + kKeys > lim;
-                // pass 1: the tile's max of the scores (raw, then scaled)
-                float mx = -INFINITY, mn = INFINITY;
+                // pass 1: the tile's extreme raw score (the max, or the min for
+                // a negative scale), four independent running values
+                float e4[4] = {masked, masked, masked, masked};
 #pragma unroll 1
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t sr[32];
                     tc::tmem_ld32(tS + ch * 32, sr);
                     tc::tmem_ld_wait();
+                    if (need_mask) {
+                        const int nv = lim - (kb + ch * 32);        // valid keys in the chunk
 #pragma unroll
-                    for (int c = 0; c < 32; ++c) {
-                        float v = __uint_as_float(sr[c]);
-                        if (need_mask && kb + ch * 32 + c >= lim) v = masked;
-                        mx = fmaxf(mx, v);
-                        mn = fminf(mn, v);
+                        for (int c = 0; c < 32; ++c)
+                            if (c >= nv) sr[c] = __float_as_uint(masked);
+                    }
+                    if (sc >= 0.f) {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            e4[0] = fmax3(e4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                            e4[1] = fmax3(e4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                            e4[2] = fmax3(e4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                            e4[3] = fmax3(e4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+                        }
+                    } else {
+#pragma unroll
+                        for (int c = 0; c < 32; c += 8) {
+                            e4[0] = fmin3(e4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
+                            e4[1] = fmin3(e4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
+                            e4[2] = fmin3(e4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
+                            e4[3] = fmin3(e4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+                        }
                     }
                 }
+                const float ext = sc >= 0.f ? fmax3(fmaxf(e4[0], e4[1]), e4[2], e4[3])
+                                            : fmin3(fminf(e4[0], e4[1]), e4[2], e4[3]);
                 // every score of the row masked: no new max (also for scale 0)
-                const float ext = sc >= 0.f ? mx : mn;
                 const float mt = ext == masked ? -INFINITY : ext * sc;
                 bool rescale = false;
                 float alpha = 1.f;
@@ -324,25 +354,30 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 }
                 const float mb = m == -INFINITY ? 0.f : m;
                 // pass 2: P = 2^(S sc - m) in bf16 over the first 64 columns
-                // (chunk ch of S -> columns 16 ch .. 16 ch + 15: already read)
+                // (chunk ch of S -> columns 16 ch .. 16 ch + 15: already read);
+                // masked keys get p = 0
+                float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll 1
                 for (int ch = 0; ch < 4; ++ch) {
                     uint32_t sr[32];
                     tc::tmem_ld32(tS + ch * 32, sr);
                     tc::tmem_ld_wait();
                     uint32_t pw[16];
+                    const int nv = need_mask ? lim - (kb + ch * 32) : 32;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        const int k = kb + ch * 32 + 2 * c;
                         float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sc, -mb));
                         float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sc, -mb));
-                        if (need_mask && k >= lim) p0 = 0.f;
-                        if (need_mask && k + 1 >= lim) p1 = 0.f;
-                        lsum += p0 + p1;
+                        if (need_mask) {
+                            p0 = 2 * c < nv ? p0 : 0.f;
+                            p1 = 2 * c + 1 < nv ? p1 : 0.f;
+                        }
+                        l4[c & 3] += p0 + p1;
                         pw[c] = pack_bf16x2(p0, p1);
                     }
                     tc::tmem_st16(tS + ch * 16, pw);
                 }
+                lsum += (l4[0] + l4[1]) + (l4[2] + l4[3]);
                 // rescale this warp's rows of O if any of them raised its max
                 if (__any_sync(0xffffffffu, rescale)) {
 #pragma unroll 1
