@@ -308,37 +308,43 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 tc::fence_after_sync();
                 const int kb = j * kKeys;
                 const bool need_mask = kb + kKeys > lim;
-                // pass 1: the tile's extreme raw score (the max, or the min for
-                // a negative scale), four independent running values
-                float e4[4] = {masked, masked, masked, masked};
-#pragma unroll 1
-                for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t sr[32];
-                    tc::tmem_ld32(tS + ch * 32, sr);
-                    tc::tmem_ld_wait();
-                    if (need_mask) {
+                // the row's 128 scores in registers (one TMEM round trip);
+                // the tile's extreme raw score (the max, or the min for a
+                // negative scale), four independent running values
+                uint32_t sr[4][32];
+#pragma unroll
+                for (int ch = 0; ch < 4; ++ch) tc::tmem_ld32(tS + ch * 32, sr[ch]);
+                tc::tmem_ld_wait();
+                if (need_mask) {
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch) {
                         const int nv = lim - (kb + ch * 32);        // valid keys in the chunk
 #pragma unroll
                         for (int c = 0; c < 32; ++c)
-                            if (c >= nv) sr[c] = __float_as_uint(masked);
+                            if (c >= nv) sr[ch][c] = __float_as_uint(masked);
                     }
-                    if (sc >= 0.f) {
+                }
+                float e4[4] = {masked, masked, masked, masked};
+                if (sc >= 0.f) {
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
-                            e4[0] = fmax3(e4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-                            e4[1] = fmax3(e4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-                            e4[2] = fmax3(e4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-                            e4[3] = fmax3(e4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+                            e4[0] = fmax3(e4[0], __uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1]));
+                            e4[1] = fmax3(e4[1], __uint_as_float(sr[ch][c + 2]), __uint_as_float(sr[ch][c + 3]));
+                            e4[2] = fmax3(e4[2], __uint_as_float(sr[ch][c + 4]), __uint_as_float(sr[ch][c + 5]));
+                            e4[3] = fmax3(e4[3], __uint_as_float(sr[ch][c + 6]), __uint_as_float(sr[ch][c + 7]));
                         }
-                    } else {
+                } else {
+#pragma unroll
+                    for (int ch = 0; ch < 4; ++ch)
 #pragma unroll
                         for (int c = 0; c < 32; c += 8) {
-                            e4[0] = fmin3(e4[0], __uint_as_float(sr[c]), __uint_as_float(sr[c + 1]));
-                            e4[1] = fmin3(e4[1], __uint_as_float(sr[c + 2]), __uint_as_float(sr[c + 3]));
-                            e4[2] = fmin3(e4[2], __uint_as_float(sr[c + 4]), __uint_as_float(sr[c + 5]));
-                            e4[3] = fmin3(e4[3], __uint_as_float(sr[c + 6]), __uint_as_float(sr[c + 7]));
+                            e4[0] = fmin3(e4[0], __uint_as_float(sr[ch][c]), __uint_as_float(sr[ch][c + 1]));
+                            e4[1] = fmin3(e4[1], __uint_as_float(sr[ch][c + 2]), __uint_as_float(sr[ch][c + 3]));
+                            e4[2] = fmin3(e4[2], __uint_as_float(sr[ch][c + 4]), __uint_as_float(sr[ch][c + 5]));
+                            e4[3] = fmin3(e4[3], __uint_as_float(sr[ch][c + 6]), __uint_as_float(sr[ch][c + 7]));
                         }
-                    }
                 }
                 const float ext = sc >= 0.f ? fmax3(fmaxf(e4[0], e4[1]), e4[2], e4[3])
                                             : fmin3(fminf(e4[0], e4[1]), e4[2], e4[3]);
@@ -353,21 +359,17 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                     m = mt;
                 }
                 const float mb = m == -INFINITY ? 0.f : m;
-                // pass 2: P = 2^(S sc - m) in bf16 over the first 64 columns
-                // (chunk ch of S -> columns 16 ch .. 16 ch + 15: already read);
-                // masked keys get p = 0
+                // P = 2^(S sc - m) in bf16 over the first 64 columns (all of S
+                // is in registers already); masked keys get p = 0
                 float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 1
+#pragma unroll
                 for (int ch = 0; ch < 4; ++ch) {
-                    uint32_t sr[32];
-                    tc::tmem_ld32(tS + ch * 32, sr);
-                    tc::tmem_ld_wait();
                     uint32_t pw[16];
                     const int nv = need_mask ? lim - (kb + ch * 32) : 32;
 #pragma unroll
                     for (int c = 0; c < 16; ++c) {
-                        float p0 = ex2(fmaf(__uint_as_float(sr[2 * c]), sc, -mb));
-                        float p1 = ex2(fmaf(__uint_as_float(sr[2 * c + 1]), sc, -mb));
+                        float p0 = ex2(fmaf(__uint_as_float(sr[ch][2 * c]), sc, -mb));
+                        float p1 = ex2(fmaf(__uint_as_float(sr[ch][2 * c + 1]), sc, -mb));
                         if (need_mask) {
                             p0 = 2 * c < nv ? p0 : 0.f;
                             p1 = 2 * c + 1 < nv ? p1 : 0.f;
@@ -560,8 +562,12 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             }
             __syncwarp();
         };
+        // one lane tests the barrier (lanes would each make their own access
+        // to the barrier word), the warp shares the answer
         auto ready = [](uint32_t b, uint32_t parity) {
-            return __shfl_sync(0xffffffffu, tc::mbar_test_wait(b, parity) ? 1 : 0, 0) != 0;
+            int r = 0;
+            if ((threadIdx.x & 31) == 0) r = tc::mbar_test_wait(b, parity) ? 1 : 0;
+            return __shfl_sync(0xffffffffu, r, 0) != 0;
         };
         // Event-driven issue for each query tile t: S_t(x) once K_x has
         // landed and PV_t(x - 1) has been issued; PV_t(y) once P_t(y) is in
