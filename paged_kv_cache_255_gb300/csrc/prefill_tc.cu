@@ -521,12 +521,11 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         // each tcgen05.mma / commit. Descriptor high word (stride offset
         // 1024 B, version, 128-byte swizzle) is common; the low word is
         // (address >> 4) | leading offset.
-        const uint32_t hi = (1024u >> 4) | (1u << 14) | (2u << 29);
-        const uint32_t lbo_k = 1u << 16;                        // K-major: 16 B (unused)
-        const uint32_t lbo_v = (kKVHalf >> 4) << 16;            // V: next 64 dims 16 KB on
-        const uint32_t q_lo = ((sbase + kOffQ) >> 4) | lbo_k;
-        const uint32_t k_lo = ((sbase + kOffK) >> 4) | lbo_k;
-        const uint32_t v_lo = ((sbase + kOffV) >> 4) | lbo_v;
+        const uint64_t dq = tc::sw128_desc(sbase + kOffQ, 16, 1024);        // K-major (LBO unused)
+        const uint64_t dk = tc::sw128_desc(sbase + kOffK, 16, 1024);
+        const uint64_t dv = tc::sw128_desc(sbase + kOffV, kKVHalf, 1024);   // MN-major: next 64 dims
+        const uint32_t hi = (uint32_t)(dq >> 32);                           // same for all three
+        const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, v_lo = (uint32_t)dv;
         auto desc = [hi](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
         // S_t = Q_t K^T from K stage st
         auto issue_s = [&](int t, int st, uint32_t release) {

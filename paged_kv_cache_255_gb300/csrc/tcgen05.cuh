@@ -189,18 +189,6 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
     asm volatile("mov.u64 %0, %%globaltimer;\n" : "=l"(t));
     return t;
 }
-// Wait for the phase with the given parity to complete; false after about
-// `limit_ns` nanoseconds without completion.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity,
-                                          uint64_t limit_ns = 2000000000ull) {
-    if (mbar_try_wait(bar, parity)) return true;
-    const uint64_t t0 = globaltimer_ns();
-    for (;;) {
-        if (mbar_try_wait_sleep(bar, parity, 100000u)) return true;
-        if (globaltimer_ns() - t0 > limit_ns) return false;
-    }
-}
-
 // -- TMA ------------------------------------------------------------------------
 // The next phase of `bar` also waits for `bytes` more bytes of asynchronous
 // copies (no arrival).
@@ -218,14 +206,6 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const void *tmap, int 
         " [%0], [%1, {%2, %3, %4}], [%5];\n" ::"r"(dst),
         "l"(reinterpret_cast<uint64_t>(tmap)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
         : "memory");
-}
-
-// Prefetch of the same box into L2 (no shared memory, no completion signal).
-__device__ __forceinline__ void tma_prefetch_3d(const void *tmap, int c0, int c1, int c2) {
-    asm volatile("cp.async.bulk.prefetch.tensor.3d.L2.global.tile [%0, {%1, %2, %3}];\n" ::"l"(
-                     reinterpret_cast<uint64_t>(tmap)),
-                 "r"(c0), "r"(c1), "r"(c2)
-                 : "memory");
 }
 
 }  // namespace tc

@@ -16,7 +16,8 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 def declared_entry_points():
     names = []
     for h in glob.glob(os.path.join(ROOT, "include", "*.h")):
-        text = open(h).read()
+        with open(h) as fh:
+            text = fh.read()
         names += re.findall(r"PA_API\s+[\w\s\*]+?\b(pa_\w+)\s*\(", text)
     return sorted(set(names))
 

@@ -42,7 +42,7 @@ def test_barrier_and_max_over_ranks_on_two_gloo_ranks():
     if torch.cuda.is_available():
         pytest.skip("the CPU (gloo) path; with a GPU bench.py picks NCCL")
     world, port = 2, _free_port()
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         results = m.dict()
         mp.spawn(_rank_main, args=(world, port, results), nprocs=world, join=True)
         assert dict(results) == {0: 15.0, 1: 15.0}

@@ -42,7 +42,8 @@ MUTANTS = [
 
 @pytest.mark.parametrize("name,old,new", MUTANTS, ids=[m[0] for m in MUTANTS])
 def test_mutant_is_caught(tmp_path, name, old, new):
-    text = open(SRC).read()
+    with open(SRC) as fh:
+        text = fh.read()
     assert old in text, f"mutation anchor for {name} not found"
     src = tmp_path / "mutant.c"
     src.write_text(text.replace(old, new))
