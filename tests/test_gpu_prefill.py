@@ -194,3 +194,38 @@ def test_rejects_bad_shapes():
     with pytest.raises(pa.PagedAttnError):      # 12 query heads over 8 KV heads
         pa.prefill(d["q"][:, :12].contiguous(), d["k_cache"], d["v_cache"],
                    d["block_tables"], d["context_lens"], d["qsl"], pb.wl.scale)
+
+
+def _random_case(rng):
+    """A seeded random prefill step: group size, block size, lengths and chunk
+    pattern drawn over the supported range."""
+    Hkv = int(rng.choice([1, 2, 4, 8]))
+    g = int(rng.choice([1, 2, 3, 4, 6, 8, 16]))
+    bs = int(rng.choice([16, 32, 64, 128, 256]))
+    S = int(rng.integers(1, 6))
+    lens, chunks = [], []
+    for _ in range(S):
+        L = int(rng.integers(0, 700))
+        kind = rng.integers(0, 4)
+        n = L if kind == 0 else (0 if kind == 1 or L == 0 else int(rng.integers(1, L + 1)))
+        lens.append(L)
+        chunks.append(n)
+    return _spec("r", g * Hkv, Hkv, bs), lens, chunks
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_random_prefill_steps(case, monkeypatch):
+    """Twelve seeded random steps, tcgen05 kernel, element-wise against the
+    oracle (and the mma.sync kernel on the same inputs)."""
+    rng = np.random.Generator(np.random.PCG64(1000 + case))
+    spec, lens, chunks = _random_case(rng)
+    pb = inputs.prefill_batch(spec, seed=2000 + case, context_lens=lens, chunk_lens=chunks)
+    kc, vc = _oracle_caches(pb)
+    ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
+                               pb.query_start_loc, pb.wl.scale)
+    for kernel in KERNELS:
+        monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
+        d = _device(pb)
+        out = _gpu_step(pb, d)
+        gu.assert_close(out, ref, f"random case {case} ({kernel}): g {spec.num_q_heads // spec.num_kv_heads} "
+                                  f"Hkv {spec.num_kv_heads} bs {spec.block_size} lens {lens} chunks {chunks}")
