@@ -562,6 +562,10 @@ def run_gpu_prefill(args, rank, world, local):
     pb = inputs.prefill_batch(spec, seed=0, chunk=chunk)
     wl = pb.wl
     k_cache, v_cache = wl.k_cache.to(dev), wl.v_cache.to(dev)
+    HM = args.layout == "head_major"
+    if HM:          # the same values in a [NB, Hkv, bs, D] pool
+        k_cache = k_cache.permute(0, 2, 1, 3).contiguous()
+        v_cache = v_cache.permute(0, 2, 1, 3).contiguous()
     host_inputs = [pb.q, pb.k_new, pb.v_new, torch.from_numpy(pb.slot_mapping),
                    torch.from_numpy(wl.block_tables), torch.from_numpy(wl.context_lens),
                    torch.from_numpy(pb.query_start_loc)]
@@ -572,8 +576,9 @@ def run_gpu_prefill(args, rank, world, local):
     stream = torch.cuda.current_stream(dev)
 
     def step(q_, kn_, vn_, sl_, bt_, cl_, qsl_):
-        pa.store_kvcache(kn_, vn_, k_cache, v_cache, sl_)
-        pa.prefill(q_, k_cache, v_cache, bt_, cl_, qsl_, wl.scale, max_query_len=mql, out=out)
+        pa.store_kvcache(kn_, vn_, k_cache, v_cache, sl_, head_major=HM)
+        pa.prefill(q_, k_cache, v_cache, bt_, cl_, qsl_, wl.scale, max_query_len=mql, out=out,
+                   head_major=HM)
 
     clocks = ClockSampler(local)
     clocks.wait_first_sample()
@@ -587,9 +592,10 @@ def run_gpu_prefill(args, rank, world, local):
     for i in range(args.steps):
         flush.zero_()
         ev[i][0].record(stream)
-        pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots)
+        pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots, head_major=HM)
         ev[i][1].record(stream)
-        pa.prefill(q, k_cache, v_cache, bt, cl, qsl, wl.scale, max_query_len=mql, out=out)
+        pa.prefill(q, k_cache, v_cache, bt, cl, qsl, wl.scale, max_query_len=mql, out=out,
+                   head_major=HM)
         ev[i][2].record(stream)
     torch.cuda.synchronize()
     barrier(world)
@@ -646,7 +652,7 @@ def run_gpu_prefill(args, rank, world, local):
         "metric": PREFILL_METRIC, "value": step_ms * 1e3, "unit": "us/step", "n_gpus": world,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": prefill_config(pb, chunk),
+        "data": "synthetic", "config": dict(prefill_config(pb, chunk), layout=args.layout),
         "store_us": store_ms * 1e3, "prefill_us": pf_ms * 1e3,
         "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
                      "frac": achieved / peak, "traffic": None, "kernel": "pa_prefill",

@@ -262,6 +262,21 @@ PA_API pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_
                               int block_size, int64_t num_blocks, void *stream);
 
 /*
+ * pa_prefill on a pool in either layout: PA_LAYOUT_TOKEN_MAJOR
+ * [NB, bs, Hkv, head_dim] (what pa_prefill takes) or PA_LAYOUT_HEAD_MAJOR
+ * [NB, Hkv, bs, head_dim] (the layout pa_store_kvcache_layout and
+ * pa_decode_layout also take). Same results for the same values in either
+ * layout; PA_ERR_INVALID_ARG for another layout value.
+ */
+PA_API pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const void *v_cache,
+                                     const int32_t *block_tables, int max_blocks_per_seq,
+                                     const int32_t *context_lens, const int32_t *query_start_loc,
+                                     int max_query_len, float scale, void *out, int num_seqs,
+                                     int total_q, int num_q_heads, int num_kv_heads, int head_dim,
+                                     int block_size, int64_t num_blocks, pa_layout_t layout,
+                                     void *stream);
+
+/*
  * Device-side error check for pa_prefill. The prefill kernel waits on the
  * tensor cores through mbarriers, each wait bounded (about 2 s); a wait that
  * runs out, or shared memory the kernel cannot align, is recorded on the

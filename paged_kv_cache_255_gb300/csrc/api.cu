@@ -223,6 +223,20 @@ pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,
                        int max_query_len, float scale, void *out, int num_seqs, int total_q,
                        int num_q_heads, int num_kv_heads, int head_dim, int block_size,
                        int64_t num_blocks, void *stream) {
+    return pa_prefill_layout(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                             query_start_loc, max_query_len, scale, out, num_seqs, total_q,
+                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                             PA_LAYOUT_TOKEN_MAJOR, stream);
+}
+
+pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, const int32_t *query_start_loc,
+                              int max_query_len, float scale, void *out, int num_seqs,
+                              int total_q, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int64_t num_blocks, pa_layout_t layout,
+                              void *stream) {
+    if (layout != PA_LAYOUT_TOKEN_MAJOR && layout != PA_LAYOUT_HEAD_MAJOR) return PA_ERR_INVALID_ARG;
     if (num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_blocks < 0 || max_blocks_per_seq < 0 || max_query_len < 0 || !std::isfinite(scale))
         return PA_ERR_INVALID_ARG;
@@ -253,6 +267,7 @@ pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,
     a.group = group;
     a.block_size_log2 = log2_exact(block_size);
     a.max_blocks_per_seq = max_blocks_per_seq;
+    a.head_major = layout == PA_LAYOUT_HEAD_MAJOR ? 1 : 0;
     a.num_blocks = num_blocks;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     const int mql = max_query_len > 0 ? max_query_len : 1;

@@ -70,6 +70,7 @@ struct PrefillArgs {
     int group;
     int block_size_log2;
     int max_blocks_per_seq;
+    int head_major;                 // pool layout [NB, Hkv, bs, 128] instead of [NB, bs, Hkv, 128]
     int64_t num_blocks;
     float scale_log2;
 };

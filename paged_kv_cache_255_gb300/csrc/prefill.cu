@@ -45,7 +45,8 @@ __device__ __forceinline__ int pf_clamp_len(const PrefillArgs &a, int s) {
 }
 
 // cp.async of the K and V rows of keys [k0, k0 + 64) of (sequence s, KV head
-// kvh) into `stage`; keys at or past kend are zero-filled.
+// kvh) into `stage`; keys at or past kend are zero-filled. Token-major pool:
+// row (slot * Hkv + kvh); head-major: ((block * Hkv + kvh) * bs + offset).
 __device__ __forceinline__ void pf_load_tile(const PrefillArgs &a, int s, int kvh, int k0,
                                              int kend, uint8_t *stage) {
     const uint32_t dst = smem_u32(stage);
@@ -61,7 +62,9 @@ __device__ __forceinline__ void pf_load_tile(const PrefillArgs &a, int s, int kv
             const int bid = __ldg(a.block_tables + (int64_t)s * a.max_blocks_per_seq +
                                   (t >> a.block_size_log2));
             ok = bid >= 0 && (int64_t)bid < a.num_blocks;
-            row = ((((int64_t)bid << a.block_size_log2) + (t & bs_mask)) * a.num_kv_heads + kvh);
+            row = a.head_major
+                      ? (((int64_t)bid * a.num_kv_heads + kvh) << a.block_size_log2) + (t & bs_mask)
+                      : ((((int64_t)bid << a.block_size_log2) + (t & bs_mask)) * a.num_kv_heads + kvh);
         }
         const int pos = chunk ^ (key & 7);
         const char *ks = static_cast<const char *>(a.k_cache) + (ok ? row * kRowBytes + chunk * 16 : 0);

@@ -20,7 +20,7 @@
 //                    O in TMEM) and sum, and writes P_j (tcgen05.st).
 //   warps 8, 9       K and V producers: per tile, 16 lanes each fetch one
 //                    box of 16 tokens x 64 dims of one KV head by TMA through
-//                    a 3-D tensor map over the pool ([NB * bs, Hkv, 128]),
+//                    a 3-D tensor map over the pool (either layout),
 //                    landing in the 128-byte swizzled layout the MMA
 //                    descriptors name, into 3 K stages and 2 V stages. V rows
 //                    of a partly used 16-token group at the end of the keys
@@ -172,11 +172,15 @@ __device__ __forceinline__ void copy_v_tail(const PrefillArgs &a, int s, int kvh
         const int t = t0 + r;
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
         if (t < kend) {
-            const int64_t row = key_row(a, s, t);
-            if (row >= 0)
+            const int64_t slot = key_row(a, s, t);
+            if (slot >= 0) {
+                const int lb = a.block_size_log2;
+                const int64_t row = a.head_major
+                    ? (((slot >> lb) * a.num_kv_heads + kvh) << lb) + (slot & ((1 << lb) - 1))
+                    : slot * a.num_kv_heads + kvh;
                 w = __ldg(reinterpret_cast<const uint4 *>(
-                    static_cast<const char *>(a.v_cache) +
-                    (row * a.num_kv_heads + kvh) * kRowBytes + chunk * 16));
+                    static_cast<const char *>(a.v_cache) + row * kRowBytes + chunk * 16));
+            }
         }
         const int key = (t0 & (kKeys - 1)) + r;     // row in the tile
         const uint32_t dst = vdst + (chunk >> 3) * kKVHalf + key * 128 +
@@ -453,18 +457,25 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x) {
             const Item it = make_item<G>(qp, n, L);
             const int kend = it.kend;
-            auto box_row = [&](int j) -> int {
+            // TMA coordinates (dim 1, dim 2) of this lane's box of tile j:
+            // token-major (KV head, slot), head-major (offset in the block,
+            // block * Hkv + KV head); dim 1 at -kGroup reads zeros (a bad block
+            // id reads as zeros that way); x = INT_MIN: no box
+            auto box_at = [&](int j) -> int2 {
                 const int k0 = j * kKeys;
                 const int ng = is_v ? groups_full(k0, kend) : groups_used(k0, kend);
-                if (lane >= 2 * kGroups || j >= it.nt || q >= ng) return INT_MIN;
-                const int64_t row = key_row(a, s, k0 + q * kGroup);
-                return row < 0 ? -kGroup : (int)row;
+                if (lane >= 2 * kGroups || j >= it.nt || q >= ng) return make_int2(INT_MIN, 0);
+                const int64_t slot = key_row(a, s, k0 + q * kGroup);
+                if (slot < 0) return a.head_major ? make_int2(-kGroup, 0) : make_int2(kvh, -kGroup);
+                if (!a.head_major) return make_int2(kvh, (int)slot);
+                const int lb = a.block_size_log2;
+                return make_int2((int)(slot & ((1 << lb) - 1)), (int)((slot >> lb) * a.num_kv_heads + kvh));
             };
-            int row_next = box_row(0);
+            int2 box_next = box_at(0);
 #pragma unroll 1
             for (int j = 0; j < it.nt; ++j) {
-                const int row = row_next;
-                row_next = box_row(j + 1);
+                const int2 box = box_next;
+                box_next = box_at(j + 1);
                 const uint32_t gj = gt + j;
                 const int st = gj % nst;
                 if (!warp_wait(bar_empty + 8 * st, ((gj / nst) & 1) ^ 1, abort)) { ok = false; break; }
@@ -474,8 +485,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 const int nk = groups_used(k0, kend), nf = groups_full(k0, kend);
                 if (lane == 0) tc::mbar_expect_tx(full, (uint32_t)(is_v ? nf : nk) * 2 * kGroup * 128);
                 __syncwarp();
-                if (row != INT_MIN)
-                    tc::tma_load_3d(dst + h * kKVHalf + q * kGroup * 128, map, h * 64, kvh, row, full);
+                if (box.x != INT_MIN)
+                    tc::tma_load_3d(dst + h * kKVHalf + q * kGroup * 128, map, h * 64, box.x, box.y, full);
                 if (is_v && nk > nf) {
                     copy_v_tail(a, s, kvh, k0 + nf * kGroup, kend, dst, lane);
                     tc::fence_proxy_async();
@@ -665,14 +676,19 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// The pool [NB, bs, Hkv, 128] as a 3-D tensor (128, Hkv, NB * bs) of bf16 with
-// 16-token boxes of 64 dims of one head, 128-byte swizzle.
-bool make_pool_map(CUtensorMap *m, const void *pool, int64_t rows, int num_kv_heads) {
+// The pool as a 3-D tensor of bf16 with boxes of 16 tokens x 64 dims of one
+// head, 128-byte swizzle: token-major [NB, bs, Hkv, 128] as (128, Hkv, NB * bs)
+// with box (64, 1, 16); head-major [NB, Hkv, bs, 128] as (128, bs, NB * Hkv)
+// with box (64, 16, 1). Either box lands as 16 rows of 128 bytes.
+bool make_pool_map(CUtensorMap *m, const void *pool, int64_t num_blocks, int block_size,
+                   int num_kv_heads, bool head_major) {
     PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
     if (!enc) return false;
-    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_kv_heads, (cuuint64_t)rows};
-    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)num_kv_heads * kRowBytes};
-    const cuuint32_t box[3] = {64, 1, (cuuint32_t)kGroup};
+    const cuuint64_t d1 = head_major ? block_size : num_kv_heads;
+    const cuuint64_t d2 = head_major ? num_blocks * num_kv_heads : num_blocks * block_size;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, d1, d2};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, d1 * kRowBytes};
+    const cuuint32_t box[3] = {64, head_major ? (cuuint32_t)kGroup : 1u, head_major ? 1u : (cuuint32_t)kGroup};
     const cuuint32_t estr[3] = {1, 1, 1};
     return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
                estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -684,11 +700,14 @@ cudaError_t launch_g(const PrefillArgs &a, int max_query_len, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<G>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
     if (e != cudaSuccess) return e;
-    const int64_t rows = a.num_blocks << a.block_size_log2;
-    if (rows >= (int64_t)1 << 31) return cudaErrorInvalidValue;    // TMA row coordinates are int32
+    // TMA coordinates are int32
+    if ((a.num_blocks << a.block_size_log2) >= (int64_t)1 << 31 ||
+        a.num_blocks * a.num_kv_heads >= (int64_t)1 << 31)
+        return cudaErrorInvalidValue;
+    const int bs = 1 << a.block_size_log2;
     CUtensorMap mk, mv;
-    if (!make_pool_map(&mk, a.k_cache, rows, a.num_kv_heads) ||
-        !make_pool_map(&mv, a.v_cache, rows, a.num_kv_heads))
+    if (!make_pool_map(&mk, a.k_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0) ||
+        !make_pool_map(&mv, a.v_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0))
         return cudaErrorInvalidValue;
     constexpr int BT = kRows / G;
     int gx = (max_query_len + 2 * BT - 1) / (2 * BT);

@@ -35,6 +35,8 @@ SIGNATURES = {
     "pa_prefill": ([_P, _P, _P, _P, _I32, _P, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                     _I32, _I64, _P], _I32),
     "pa_take_device_error": ([_P, _P], _I32),
+    "pa_prefill_layout": ([_P, _P, _P, _P, _I32, _P, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32,
+                           _I32, _I32, _I64, _I32, _P], _I32),
     "pa_store_kvcache_layout": ([_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64, _I32, _P],
                                 _I32),
     "pa_decode_layout": ([_P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32, _I32, _I32, _I64,
@@ -245,11 +247,12 @@ def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out=Non
 
 
 def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, scale,
-            max_query_len=None, out=None, stream=None):
+            max_query_len=None, out=None, stream=None, head_major=False):
     """Paged prefill: q is bf16 [total_q, Hq, D], rows packed per sequence by
     query_start_loc (int32 [S + 1]); row i of sequence s sits at position
     context_lens[s] - n_s + i and attends causally to the sequence's cached
-    tokens. Returns out [total_q, Hq, D]."""
+    tokens. The pool is [NB, bs, Hkv, D], or [NB, Hkv, bs, D] with
+    head_major=True. Returns out [total_q, Hq, D]."""
     dev = q.device
     for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
                      (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
@@ -257,7 +260,10 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, sc
                      (query_start_loc, "query_start_loc", torch.int32)):
         _cuda(t, n, dt, dev)
     T, Hq, D = q.shape
-    NB, bs, Hkv, D2 = k_cache.shape
+    if head_major:
+        NB, Hkv, bs, D2 = k_cache.shape
+    else:
+        NB, bs, Hkv, D2 = k_cache.shape
     S = context_lens.shape[0]
     if v_cache.shape != k_cache.shape or D2 != D or block_tables.dim() != 2 \
             or block_tables.shape[0] != S or query_start_loc.shape != (S + 1,):
@@ -271,12 +277,13 @@ def prefill(q, k_cache, v_cache, block_tables, context_lens, query_start_loc, sc
         if out.shape != q.shape:
             raise ValueError("out must have q's shape")
     with torch.cuda.device(dev):
-        st = lib().pa_prefill(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                              block_tables.data_ptr(), block_tables.shape[1],
-                              context_lens.data_ptr(), query_start_loc.data_ptr(),
-                              int(max_query_len), float(scale), out.data_ptr(), S, T, Hq, Hkv, D,
-                              bs, NB, _stream_ptr(stream, dev))
-    _check("pa_prefill", st)
+        st = lib().pa_prefill_layout(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                     block_tables.data_ptr(), block_tables.shape[1],
+                                     context_lens.data_ptr(), query_start_loc.data_ptr(),
+                                     int(max_query_len), float(scale), out.data_ptr(), S, T, Hq,
+                                     Hkv, D, bs, NB, 1 if head_major else 0,
+                                     _stream_ptr(stream, dev))
+    _check("pa_prefill_layout", st)
     return out
 
 

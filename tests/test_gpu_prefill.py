@@ -229,3 +229,34 @@ def test_random_prefill_steps(case, monkeypatch):
         out = _gpu_step(pb, d)
         gu.assert_close(out, ref, f"random case {case} ({kernel}): g {spec.num_q_heads // spec.num_kv_heads} "
                                   f"Hkv {spec.num_kv_heads} bs {spec.block_size} lens {lens} chunks {chunks}")
+
+
+LAYOUT_CASES = [
+    ("g4_mixed", _spec("a", 8, 2, 16), [37, 200, 16, 129, 5], [37, 64, 1, 100, 5]),
+    ("g2_bs64", _spec("l", 16, 8, 64), [300, 77, 600], [150, 77, 333]),
+    ("g8_bs256", _spec("m", 64, 8, 256), [520, 33], [520, 10]),
+]
+
+
+@pytest.mark.parametrize("kernel", KERNELS)
+@pytest.mark.parametrize("name,spec,lens,chunks", LAYOUT_CASES, ids=[c[0] for c in LAYOUT_CASES])
+def test_head_major_pool(name, spec, lens, chunks, kernel, monkeypatch):
+    """The step on a head-major pool [NB, Hkv, bs, D] (store and prefill both
+    head-major) matches the oracle, and the prefill gives the same bits as on
+    the token-major pool holding the same values."""
+    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
+    pb = inputs.prefill_batch(spec, seed=67, context_lens=lens, chunk_lens=chunks)
+    kc, vc = _oracle_caches(pb)
+    ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
+                               pb.query_start_loc, pb.wl.scale)
+    d = _device(pb)
+    k_hm = d["k_cache"].permute(0, 2, 1, 3).contiguous()
+    v_hm = d["v_cache"].permute(0, 2, 1, 3).contiguous()
+    pa.store_kvcache(d["k_new"], d["v_new"], k_hm, v_hm, d["slot_mapping"], head_major=True)
+    out_hm = pa.prefill(d["q"], k_hm, v_hm, d["block_tables"], d["context_lens"], d["qsl"],
+                        pb.wl.scale, head_major=True)
+    out_tm = _gpu_step(pb, d)
+    torch.cuda.synchronize()
+    gu.assert_close(out_hm, ref, f"{name} head-major ({kernel})")
+    assert torch.equal(out_hm.view(torch.int16), out_tm.view(torch.int16))
+    assert torch.equal(k_hm.permute(0, 2, 1, 3).view(torch.int16), d["k_cache"].view(torch.int16))
