@@ -287,6 +287,15 @@ PA_API pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const v
  */
 PA_API pa_status_t pa_take_device_error(int32_t *code, void *stream);
 
+/*
+ * Test hook for the error path above, off by default: with mode 1, later
+ * pa_prefill / pa_prefill_layout launches (tcgen05 kernel) hold back one
+ * barrier arrival of their V producer, so that a wait runs out after about 2 s
+ * and the launch records code 2 and returns, its outputs undefined; mode 0
+ * restores normal launches. Process-wide; for tests only.
+ */
+PA_API pa_status_t pa_debug_prefill_fault(int mode);
+
 #ifdef __cplusplus
 }
 #endif

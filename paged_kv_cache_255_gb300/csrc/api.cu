@@ -268,6 +268,7 @@ pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const void *v_
     a.block_size_log2 = log2_exact(block_size);
     a.max_blocks_per_seq = max_blocks_per_seq;
     a.head_major = layout == PA_LAYOUT_HEAD_MAJOR ? 1 : 0;
+    a.fault_hold_v = pa::prefill_fault();
     a.num_blocks = num_blocks;
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     const int mql = max_query_len > 0 ? max_query_len : 1;
@@ -276,6 +277,12 @@ pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const void *v_
     const cudaError_t e = (k && std::strcmp(k, "mma") == 0) ? pa::launch_prefill(a, gp, mql, st)
                                                             : pa::launch_prefill_tc(a, gp, mql, st);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
+}
+
+pa_status_t pa_debug_prefill_fault(int mode) {
+    if (mode != 0 && mode != 1) return PA_ERR_INVALID_ARG;
+    pa::set_prefill_fault(mode);
+    return PA_OK;
 }
 
 pa_status_t pa_take_device_error(int32_t *code, void *stream) {

@@ -71,9 +71,17 @@ struct PrefillArgs {
     int block_size_log2;
     int max_blocks_per_seq;
     int head_major;                 // pool layout [NB, Hkv, bs, 128] instead of [NB, bs, Hkv, 128]
+    int fault_hold_v;               // test hook, normally 0: see set_prefill_fault
     int64_t num_blocks;
     float scale_log2;
 };
+
+// Test hook for the bounded waits of the tcgen05 prefill kernel: with mode 1
+// its V producer leaves the first tile's v_full barrier without its arrival,
+// so the MMA warp's wait for it runs out (about 2 s), the kernel records error
+// 2 and every warp exits. Mode 0 (the default) turns it off.
+void set_prefill_fault(int mode);
+int prefill_fault();
 
 cudaError_t launch_prefill(const PrefillArgs &a, int group_pad, int max_query_len,
                            cudaStream_t stream);

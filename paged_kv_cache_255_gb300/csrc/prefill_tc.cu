@@ -45,6 +45,7 @@
 // bounded (about 2 s) and also gives up once any thread of the CTA has
 // recorded a failed wait; then every role skips to the end, where the CTA
 // frees its TMEM and exits.
+#include <atomic>
 #include <climits>
 #include <cmath>
 #include <mutex>
@@ -491,7 +492,9 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                     copy_v_tail(a, s, kvh, k0 + nf * kGroup, kend, dst, lane);
                     tc::fence_proxy_async();
                 }
-                warp_arrive(full);
+                // (test hook: the first tile's V arrival held back, see
+                // set_prefill_fault)
+                if (!(is_v && a.fault_hold_v && gj == 0)) warp_arrive(full);
             }
             gt += it.nt;
         }
@@ -729,6 +732,13 @@ cudaError_t launch_prefill_tc(const PrefillArgs &a, int group_pad, int max_query
         default: return cudaErrorInvalidValue;
     }
 }
+
+namespace {
+std::atomic<int> g_fault_mode{0};
+}  // namespace
+
+void set_prefill_fault(int mode) { g_fault_mode.store(mode); }
+int prefill_fault() { return g_fault_mode.load(); }
 
 cudaError_t take_prefill_error(cudaStream_t stream, int *code) {
     int v = 0;

@@ -35,6 +35,7 @@ SIGNATURES = {
     "pa_prefill": ([_P, _P, _P, _P, _I32, _P, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                     _I32, _I64, _P], _I32),
     "pa_take_device_error": ([_P, _P], _I32),
+    "pa_debug_prefill_fault": ([_I32], _I32),
     "pa_prefill_layout": ([_P, _P, _P, _P, _I32, _P, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32,
                            _I32, _I32, _I64, _I32, _P], _I32),
     "pa_store_kvcache_layout": ([_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64, _I32, _P],
@@ -297,6 +298,13 @@ def take_device_error(stream=None, device=None) -> int:
         st = lib().pa_take_device_error(ctypes.addressof(code), _stream_ptr(stream, dev))
     _check("pa_take_device_error", st)
     return int(code.value)
+
+
+def debug_prefill_fault(mode: int) -> None:
+    """Test hook (off by default): mode 1 makes later prefill launches hold back
+    one barrier arrival so that a bounded wait runs out and code 2 is recorded;
+    mode 0 turns it off."""
+    _check("pa_debug_prefill_fault", lib().pa_debug_prefill_fault(int(mode)))
 
 
 class DecodeStepGraph:

@@ -1,6 +1,8 @@
 """Paged prefill through the C ABI against the fp64 oracle: each sequence's
 chunk of new rows is stored through its slot mapping, then row i of a chunk of
 n in a sequence of L attends to keys t <= L - n + i."""
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -260,3 +262,32 @@ def test_head_major_pool(name, spec, lens, chunks, kernel, monkeypatch):
     gu.assert_close(out_hm, ref, f"{name} head-major ({kernel})")
     assert torch.equal(out_hm.view(torch.int16), out_tm.view(torch.int16))
     assert torch.equal(k_hm.permute(0, 2, 1, 3).view(torch.int16), d["k_cache"].view(torch.int16))
+
+
+def test_bounded_wait_runs_out_and_reports():
+    """The tcgen05 kernel's waits are bounded: with the test hook holding back
+    one barrier arrival, the launch returns after about 2 s with code 2 instead
+    of hanging, and the context stays usable (the next launch is correct)."""
+    spec = _spec("t", 2, 1, 16)
+    pb = inputs.prefill_batch(spec, seed=68, context_lens=[100], chunk_lens=[100])
+    d = _device(pb)
+    pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+    torch.cuda.synchronize()
+    pa.debug_prefill_fault(1)
+    try:
+        t0 = time.time()
+        pa.prefill(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                   d["qsl"], pb.wl.scale)
+        torch.cuda.synchronize()
+        dt = time.time() - t0
+    finally:
+        pa.debug_prefill_fault(0)
+    assert pa.take_device_error() == 2
+    assert 1.0 < dt < 60.0, dt
+    kc, vc = _oracle_caches(pb)
+    ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
+                               pb.query_start_loc, pb.wl.scale)
+    out = pa.prefill(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                     d["qsl"], pb.wl.scale)
+    torch.cuda.synchronize()
+    gu.assert_close(out, ref, "after a timed-out launch")
