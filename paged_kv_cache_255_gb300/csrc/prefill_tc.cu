@@ -141,8 +141,21 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 }
 
 // Warp-level hand-offs: one lane waits (or arrives) for the whole warp, the
-// others are ordered with it by __syncwarp.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort) {
+// others are ordered with it by __syncwarp. With `spin` (the waits on the
+// per-tile chain), the warp first polls: every lane tests the barrier (one
+// shared-memory access, no divergent branch), a vote gives one answer and
+// __syncwarp orders the lanes that saw the phase complete before the rest.
+// A thread that try_wait has suspended resumes some hundreds of cycles after
+// the phase completes, which those hand-offs cannot afford.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int *abort,
+                                          bool spin = false) {
+    if (spin) {
+        for (int i = 0; i < 256; ++i)
+            if (__any_sync(0xffffffffu, tc::mbar_test_wait(bar, parity))) {
+                __syncwarp();
+                return true;
+            }
+    }
     bool ok = true;
     if ((threadIdx.x & 31) == 0) ok = wait_bar(bar, parity, abort);
     const bool r = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
@@ -309,7 +322,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             for (int j = 0; j < it.nt; ++j) {
                 const uint32_t gj = gt + j;
                 // S_t(j) done: also PV_t(j - 1) (issued before it), so O is stable
-                if (!warp_wait(bar(kBarSFull + wg), gj & 1, abort)) { ok = false; break; }
+                if (!warp_wait(bar(kBarSFull + wg), gj & 1, abort, true)) { ok = false; break; }
                 tc::fence_after_sync();
                 const int kb = j * kKeys;
                 const bool need_mask = kb + kKeys > lim;
@@ -405,7 +418,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             if (!ok) break;
             // epilogue: O / l -> bf16 rows; then O is free for the next item
             if (it.nt > 0) {
-                if (!warp_wait(bar(kBarPVDone + wg), (gt + it.nt - 1) & 1, abort)) { ok = false; break; }
+                if (!warp_wait(bar(kBarPVDone + wg), (gt + it.nt - 1) & 1, abort, true)) { ok = false; break; }
                 tc::fence_after_sync();
             }
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -575,12 +588,15 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             }
             __syncwarp();
         };
-        // one lane tests the barrier (lanes would each make their own access
-        // to the barrier word), the warp shares the answer
+        // every lane tests the barrier (one shared-memory access for the
+        // warp, no divergent branch) and a vote gives the warp one answer: a
+        // completed phase stays completed until this warp issues the work
+        // that lets the next one complete, so any lane's yes is the answer;
+        // __syncwarp then orders the lanes that saw it before the others
         auto ready = [](uint32_t b, uint32_t parity) {
-            int r = 0;
-            if ((threadIdx.x & 31) == 0) r = tc::mbar_test_wait(b, parity) ? 1 : 0;
-            return __shfl_sync(0xffffffffu, r, 0) != 0;
+            const bool r = __any_sync(0xffffffffu, tc::mbar_test_wait(b, parity));
+            if (r) __syncwarp();
+            return r;
         };
         // Event-driven issue for each query tile t: S_t(x) once K_x has
         // landed and PV_t(x - 1) has been issued; PV_t(y) once P_t(y) is in
@@ -633,8 +649,9 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                     idle = 0;
                     continue;
                 }
-                // nothing ready: back off briefly
-                __nanosleep(32);
+                // nothing ready: poll again (no back-off: a sleeping issuer
+                // reacts late to the next hand-off); the 2 s limit is
+                // checked every 256 rounds
                 if (++idle == 1) {
                     t_idle = tc::globaltimer_ns();
                 } else if ((idle & 255) == 0) {
