@@ -104,6 +104,7 @@ constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, kKeys, false);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, true);
 constexpr float kRescaleSlack = 8.f;                    // log2 units
+constexpr int kPairsPerCta = 1;                         // query-tile pairs per CTA (grid sizing)
 
 enum : int { kErrSmemAlign = 1, kErrTimeout = 2 };
 
@@ -224,6 +225,16 @@ struct Item {
     int nt;         // K/V tiles
 };
 
+// Pair index of the i-th item of CTA b of the g CTAs of a (sequence, KV
+// head), or -1 past the last: the np pairs, heaviest first (the last rows of
+// the chunk see the most keys), are dealt in boustrophedon order b, 2g-1-b,
+// 2g+b, ... so that each CTA's pairs add up to about the same work. Over b in
+// [0, g) the positions cover [0, np) once each, whatever g is.
+__device__ __forceinline__ int pair_of(int i, int b, int g, int np) {
+    const int pos = 2 * g * (i >> 1) + ((i & 1) ? 2 * g - 1 - b : b);
+    return pos < np ? np - 1 - pos : -1;
+}
+
 template <int G>
 __device__ __forceinline__ Item make_item(int qp, int n, int L) {
     constexpr int BT = kRows / G;
@@ -251,10 +262,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
     q0 = q0 < 0 ? 0 : (q0 > a.total_q ? a.total_q : q0);
     q1 = q1 < q0 ? q0 : (q1 > a.total_q ? a.total_q : q1);
     const int n = q1 - q0;
-    // pairs qp_first, qp_first + gridDim.x, ...; the heaviest (last rows of
-    // the chunk see the most keys) first
-    const int qp_first = gridDim.x - 1 - blockIdx.x;
-    if (qp_first * 2 * BT >= n) return;
+    const int np = (n + 2 * BT - 1) / (2 * BT);            // query-tile pairs of the chunk
+    if (pair_of(0, blockIdx.x, gridDim.x, np) < 0) return;
 
     const uint32_t sbase = smem_u32(smem);
     if (sbase & 1023u) {                        // the swizzle atoms need 1024-byte alignment
@@ -308,7 +317,9 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         uint32_t gt = 0;                        // tiles done before this item
         bool ok = true;
 #pragma unroll 1
-        for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x) {
+        for (int i = 0; ok; ++i) {
+            const int qp = pair_of(i, blockIdx.x, gridDim.x, np);
+            if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             const int tok = it.tok0 + wg * BT + r / G, head = r % G;
             const bool rv = tok < n && head < g;
@@ -468,7 +479,9 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         uint32_t gt = 0;
         bool ok = true;
 #pragma unroll 1
-        for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x) {
+        for (int i = 0; ok; ++i) {
+            const int qp = pair_of(i, blockIdx.x, gridDim.x, np);
+            if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             const int kend = it.kend;
             // TMA coordinates (dim 1, dim 2) of this lane's box of tile j:
@@ -518,7 +531,9 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         int item = 0;
         bool ok = true;
 #pragma unroll 1
-        for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x, ++item) {
+        for (int i = 0; ok; ++i, ++item) {
+            const int qp = pair_of(i, blockIdx.x, gridDim.x, np);
+            if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             if (item > 0 && !warp_wait(bar(kBarQEmpty), (item - 1) & 1, abort)) { ok = false; break; }
             // Q_A and Q_B: row r of the pair is token tok0 + r / G, head r % G
@@ -607,7 +622,9 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         int item = 0;
         bool ok = true;
 #pragma unroll 1
-        for (int qp = qp_first; ok && qp * 2 * BT < n; qp += gridDim.x, ++item) {
+        for (int i = 0; ok; ++i, ++item) {
+            const int qp = pair_of(i, blockIdx.x, gridDim.x, np);
+            if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             ok = warp_wait(bar(kBarQFull), item & 1, abort);
             int sj0 = 0, sj1 = 0, pj0 = 0, pj1 = 0;     // next S / PV tile of A, B
@@ -730,7 +747,8 @@ cudaError_t launch_g(const PrefillArgs &a, int max_query_len, cudaStream_t st) {
         !make_pool_map(&mv, a.v_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0))
         return cudaErrorInvalidValue;
     constexpr int BT = kRows / G;
-    int gx = (max_query_len + 2 * BT - 1) / (2 * BT);
+    const int pairs = (max_query_len + 2 * BT - 1) / (2 * BT);
+    int gx = (pairs + kPairsPerCta - 1) / kPairsPerCta;
     gx = gx < 1 ? 1 : (gx > 65535 ? 65535 : gx);
     prefill_tc_kernel<G><<<dim3(gx, a.num_seqs, a.num_kv_heads), kThreads, kSmemBytes, st>>>(a, mk, mv);
     return cudaGetLastError();
