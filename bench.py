@@ -219,8 +219,9 @@ def oracle_sample(wl, target_s: float, host=None):
     decode_s = elapsed * (work_all / max(done_work, 1.0))
     us = (t_store + decode_s) * 1e6
     sample = (f"oracle store of all {int(wl.slot_mapping.shape[0])} rows + decode of "
-              f"{done_pairs} random (seq, q-head) outputs out of {S * Hq} per step "
-              f"({elapsed:.1f} s of oracle time), scaled by context tokens to one full step")
+              f"{done_pairs} (seq, q-head) outputs drawn at random with repeats (one step "
+              f"has {S * Hq}), {elapsed:.1f} s of oracle time, scaled by context tokens "
+              f"to one full step")
     return us, threads, sample
 
 
