@@ -43,6 +43,7 @@ namespace {
 constexpr int kWarps = 4;      // workers per CTA
 constexpr int kStages = 3;     // tiles in flight per worker (ring depth)
 constexpr int kStageBytes = 2 * kTileBytes;   // K tile then V tile
+constexpr int kCombineBatch = 8;              // pieces a combine warp loads at once
 constexpr float kNegInf = -INFINITY;
 
 __device__ __forceinline__ int clamp_len(const int32_t *cl, int s, int max_len) {
@@ -678,7 +679,9 @@ decode_kernel(const DecodeArgs a) {
 // Log-sum-exp merge of the pieces of each split unit. Block (x, y) holds
 // four warps, one per worker task 4x .. 4x + 3, all on column y; lane l
 // handles dims [4l, 4l + 4). One online pass over the pieces: each piece's
-// (max, sum, o) is folded in with weights 2^(m_i - M).
+// (max, sum, o) is folded in with weights 2^(m_i - M). The pieces are read
+// in batches whose loads are all issued before the batch is merged, so that
+// a unit cut into n pieces costs about n / kCombineBatch memory round trips.
 template <int GP>
 __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     // programmatic dependent of the decode grid: wait for all of it (and its
@@ -693,20 +696,34 @@ __global__ void __launch_bounds__(128) combine_kernel(const DecodeArgs a) {
     const int n = 1 + task.w - w;
     const float2 *ml = reinterpret_cast<const float2 *>(a.part_ml);
     float M = kNegInf, L = 0.f, acc0 = 0.f, acc1 = 0.f, acc2 = 0.f, acc3 = 0.f;
-#pragma unroll 4
-    for (int i = 0; i < n; ++i) {
-        const int slot = i == 0 ? task.z : 2 * (w + i);
-        const float2 e = ml[(int64_t)slot * GP + h];
-        const float4 po = reinterpret_cast<const float4 *>(a.part_o + ((int64_t)slot * GP + h) * kHeadDim)[lane];
-        if (e.x == kNegInf) continue;        // no visible token of this column in the piece
-        const float Mn = fmaxf(M, e.x);
-        const float a_old = ex2(M - Mn), a_new = ex2(e.x - Mn);
-        L = L * a_old + e.y * a_new;
-        acc0 = acc0 * a_old + po.x * a_new;
-        acc1 = acc1 * a_old + po.y * a_new;
-        acc2 = acc2 * a_old + po.z * a_new;
-        acc3 = acc3 * a_old + po.w * a_new;
-        M = Mn;
+    // pieces in batches: a batch's loads are all in flight before its merge
+    for (int i0 = 0; i0 < n; i0 += kCombineBatch) {
+        float2 eb[kCombineBatch];
+        float4 ob[kCombineBatch];
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k) {
+            const int i = i0 + k;
+            if (i < n) {
+                const int slot = i == 0 ? task.z : 2 * (w + i);
+                eb[k] = ml[(int64_t)slot * GP + h];
+                ob[k] = reinterpret_cast<const float4 *>(a.part_o + ((int64_t)slot * GP + h) * kHeadDim)[lane];
+            }
+        }
+#pragma unroll
+        for (int k = 0; k < kCombineBatch; ++k) {
+            if (i0 + k >= n) break;
+            const float2 e = eb[k];
+            const float4 po = ob[k];
+            if (e.x == kNegInf) continue;    // no visible token of this column in the piece
+            const float Mn = fmaxf(M, e.x);
+            const float a_old = ex2(M - Mn), a_new = ex2(e.x - Mn);
+            L = L * a_old + e.y * a_new;
+            acc0 = acc0 * a_old + po.x * a_new;
+            acc1 = acc1 * a_old + po.y * a_new;
+            acc2 = acc2 * a_old + po.z * a_new;
+            acc3 = acc3 * a_old + po.w * a_new;
+            M = Mn;
+        }
     }
     const float inv = L > 0.f ? 1.f / L : 0.f;
     uint2 pk;
