@@ -93,3 +93,17 @@ def test_random_decode_step(case):
         assert np.array_equal(gu.host_bits(gkc), kc), what
         assert np.array_equal(gu.host_bits(gvc), vc), what
     gu.assert_close(out, ref, what)
+
+
+def test_many_short_sequences():
+    """3000 sequences of 0..40 tokens: the share planning scans the lengths in
+    several chunks, and warps cross many small units."""
+    lens = np.random.default_rng(77).integers(0, 41, 3000).astype(np.int32)
+    spec = inputs.Spec("many", ((3000, 1, 1),), 32, 8, 16, pool_factor=1.2)
+    wl = inputs.generate(spec, seed=3, context_lens=lens)
+    O = oracle.get()
+    kc, vc = O.store_kvcache(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping)
+    ref = O.decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+    out, gkc, gvc = gu.gpu_step(wl)
+    assert np.array_equal(gu.host_bits(gkc), kc) and np.array_equal(gu.host_bits(gvc), vc)
+    gu.assert_close(out, ref, "3000 short sequences")

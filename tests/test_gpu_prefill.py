@@ -21,6 +21,8 @@ def _spec(name, Hq, Hkv, bs):
     return inputs.Spec(name, ((1, 1, 1),), Hq, Hkv, bs, store_mode="none")
 
 
+_MANY = [int(x) for x in np.random.default_rng(5).integers(1, 41, 300)]
+
 # (id, spec, chunk, context_lens, chunk_lens)
 CASES = [
     ("g4_mixed", _spec("a", 8, 2, 16), None, [37, 200, 16, 129, 5], [37, 64, 1, 100, 5]),
@@ -34,6 +36,8 @@ CASES = [
     ("g5_pad8", _spec("f", 40, 8, 128), None, [400, 9], [131, 9]),
     ("empty_chunks", _spec("g", 16, 8, 16), None, [0, 5, 16, 64, 65, 3],
      [0, 0, 16, 1, 65, 3]),
+    # many short whole prompts: 300 sequences of 1..40 tokens (one CTA row per sequence)
+    ("many_short", _spec("h", 16, 4, 16), None, _MANY, _MANY),
 ]
 
 
