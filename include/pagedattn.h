@@ -277,13 +277,23 @@ PA_API pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const v
                                      void *stream);
 
 /*
- * Device-side error check for pa_prefill. The prefill kernel waits on the
- * tensor cores through mbarriers, each wait bounded (about 2 s); a wait that
- * runs out, or shared memory the kernel cannot align, is recorded on the
- * device instead of hanging. This call synchronizes `stream`, stores the first
- * recorded code in *code (0 = none, 1 = shared memory misaligned, 2 = a wait
- * ran out; the outputs of the affected launch are then undefined) and clears
- * it.
+ * Device-side error record. The kernels do not fault or hang on their inputs:
+ * an index outside its range is handled in a defined way, and the prefill
+ * kernel's waits on the tensor cores through mbarriers are bounded (about
+ * 2 s). Each such event is recorded on the device, the first code of each
+ * kernel kind kept, without any synchronization in the calls themselves.
+ * This call synchronizes `stream`, stores the smallest recorded code in *code
+ * and clears every record:
+ *   0  none;
+ *   1  pa_prefill: shared memory not 1024-byte aligned; the launch's outputs
+ *      are undefined;
+ *   2  pa_prefill: a bounded wait ran out; the launch's outputs are undefined;
+ *   3  pa_store_kvcache: a slot outside [-1, num_blocks * block_size) was
+ *      skipped; nothing is written for that row;
+ *   4  pa_decode / pa_decode_multi / pa_prefill: a block-table entry that
+ *      covers context tokens lies outside [0, num_blocks); its rows are read
+ *      as zeros, so each of those keys scores 0 and adds a zero value.
+ * Entries past a sequence's last block are never read and never reported.
  */
 PA_API pa_status_t pa_take_device_error(int32_t *code, void *stream);
 

@@ -287,10 +287,17 @@ pa_status_t pa_debug_prefill_fault(int mode) {
 
 pa_status_t pa_take_device_error(int32_t *code, void *stream) {
     if (!code) return PA_ERR_INVALID_ARG;
-    int v = 0;
-    if (pa::take_prefill_error(static_cast<cudaStream_t>(stream), &v) != cudaSuccess)
-        return PA_ERR_CUDA;
-    *code = v;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    cudaError_t (*const take[])(cudaStream_t, int *) = {
+        pa::take_prefill_error, pa::take_prefill_mma_error, pa::take_decode_error,
+        pa::take_store_error};
+    int first = 0;
+    for (auto f : take) {   // every word is read and cleared; the smallest code is reported
+        int v = 0;
+        if (f(st, &v) != cudaSuccess) return PA_ERR_CUDA;
+        if (v != 0 && (first == 0 || v < first)) first = v;
+    }
+    *code = first;
     return PA_OK;
 }
 

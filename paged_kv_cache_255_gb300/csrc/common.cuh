@@ -11,6 +11,34 @@ constexpr int kTileTokens = 16;                  // tokens per KV tile
 constexpr int kRowBytes = kHeadDim * 2;          // one bf16 K (or V) row: 256 B
 constexpr int kTileBytes = kTileTokens * kRowBytes;  // 4 KB
 
+// Device-side error codes. Each kernel file keeps a __device__ int word that
+// a kernel sets (first code wins) when it meets one of these and carries on
+// in the defined way; pa_take_device_error reads and clears the words.
+enum DeviceError : int {
+    kErrNone = 0,
+    kErrSmemAlign = 1,   // prefill: dynamic shared memory not 1024-byte aligned; CTA skipped
+    kErrTimeout = 2,     // prefill: a bounded mbarrier wait ran out; the launch gave up
+    kErrBadSlot = 3,     // store: a slot outside [-1, num_blocks * block_size) was skipped
+    kErrBadBlock = 4,    // decode / prefill: a block id outside [0, num_blocks) read as zeros
+};
+
+// Read the __device__ int `word` (of the calling file) on `stream`, wait for
+// it, store it in *code and clear it if it was set.
+template <typename Word>
+inline cudaError_t take_device_word(Word &word, cudaStream_t stream, int *code) {
+    int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, word, sizeof(int), 0, cudaMemcpyDeviceToHost, stream);
+    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    if (e != cudaSuccess) return e;
+    *code = v;
+    if (v != 0) {
+        const int zero = 0;
+        e = cudaMemcpyToSymbolAsync(word, &zero, sizeof(int), 0, cudaMemcpyHostToDevice, stream);
+        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+    }
+    return e;
+}
+
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -38,6 +38,8 @@
 
 namespace pa {
 
+__device__ int g_decode_error;       // first device-side error of a decode launch
+
 namespace {
 
 constexpr int kWarps = 4;      // workers per CTA
@@ -100,7 +102,10 @@ template <bool SWZ>
 __device__ __forceinline__ void issue_tile(const Cursor &c, int bid, uint8_t *stage,
                                            const DecodeArgs &a, int lane) {
     int valid = tile_valid(c);
-    if (bid < 0 || (int64_t)bid >= a.num_blocks) valid = 0;   // never address outside the pool
+    if (bid < 0 || (int64_t)bid >= a.num_blocks) {   // never address outside the pool
+        if (valid > 0 && lane == 0) atomicCAS(&g_decode_error, 0, kErrBadBlock);
+        valid = 0;
+    }
     const int off = (c.j << 4) & ((1 << a.block_size_log2) - 1);
     // token-major pool [NB][bs][Hkv][D]: a tile's rows are Hkv rows apart;
     // head-major pool [NB][Hkv][bs][D]: they are one contiguous run
@@ -806,6 +811,10 @@ cudaError_t launch_for<16>(const DecodeArgs &a, DecodeKernel, cudaStream_t st) {
 }
 
 }  // namespace
+
+cudaError_t take_decode_error(cudaStream_t stream, int *code) {
+    return take_device_word(g_decode_error, stream, code);
+}
 
 int decode_group_pad(int group) {
     if (group < 1) return 0;

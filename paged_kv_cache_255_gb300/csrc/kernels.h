@@ -90,9 +90,12 @@ cudaError_t launch_prefill(const PrefillArgs &a, int group_pad, int max_query_le
 // take_prefill_error.
 cudaError_t launch_prefill_tc(const PrefillArgs &a, int group_pad, int max_query_len,
                               cudaStream_t stream);
-// Synchronizes the stream, returns the first recorded error code (0 = none)
-// and clears it.
+// Each synchronizes the stream, returns the first code its kernels recorded
+// (DeviceError in common.cuh; 0 = none) and clears it.
 cudaError_t take_prefill_error(cudaStream_t stream, int *code);
+cudaError_t take_prefill_mma_error(cudaStream_t stream, int *code);
+cudaError_t take_decode_error(cudaStream_t stream, int *code);
+cudaError_t take_store_error(cudaStream_t stream, int *code);
 
 cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
                                  const int64_t *slot_mapping, int64_t num_tokens,

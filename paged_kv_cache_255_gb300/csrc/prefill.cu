@@ -27,6 +27,8 @@
 
 namespace pa {
 
+__device__ int g_prefill_mma_error;  // first device-side error of a launch of this kernel
+
 namespace {
 
 constexpr int kPfRows = 64;                    // query rows per CTA
@@ -62,6 +64,7 @@ __device__ __forceinline__ void pf_load_tile(const PrefillArgs &a, int s, int kv
             const int bid = __ldg(a.block_tables + (int64_t)s * a.max_blocks_per_seq +
                                   (t >> a.block_size_log2));
             ok = bid >= 0 && (int64_t)bid < a.num_blocks;
+            if (!ok) atomicCAS(&g_prefill_mma_error, 0, kErrBadBlock);   // read as zeros
             row = a.head_major
                       ? (((int64_t)bid * a.num_kv_heads + kvh) << a.block_size_log2) + (t & bs_mask)
                       : ((((int64_t)bid << a.block_size_log2) + (t & bs_mask)) * a.num_kv_heads + kvh);
@@ -272,6 +275,10 @@ cudaError_t launch_prefill_g(const PrefillArgs &a, int max_query_len, cudaStream
 }
 
 }  // namespace
+
+cudaError_t take_prefill_mma_error(cudaStream_t stream, int *code) {
+    return take_device_word(g_prefill_mma_error, stream, code);
+}
 
 cudaError_t launch_prefill(const PrefillArgs &a, int group_pad, int max_query_len,
                            cudaStream_t stream) {

@@ -106,8 +106,6 @@ constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, true);
 constexpr float kRescaleSlack = 8.f;                    // log2 units
 constexpr int kPairsPerCta = 1;                         // query-tile pairs per CTA (grid sizing)
 
-enum : int { kErrSmemAlign = 1, kErrTimeout = 2 };
-
 __device__ __forceinline__ void set_error(int code) { atomicCAS(&g_prefill_error, 0, code); }
 
 // Three-input max / min (one instruction on sm_100-family parts).
@@ -171,7 +169,10 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
 // Physical row (token slot) of key t of sequence s in the pool, or -1.
 __device__ __forceinline__ int64_t key_row(const PrefillArgs &a, int s, int t) {
     const int bid = __ldg(a.block_tables + (int64_t)s * a.max_blocks_per_seq + (t >> a.block_size_log2));
-    if (bid < 0 || (int64_t)bid >= a.num_blocks) return -1;
+    if (bid < 0 || (int64_t)bid >= a.num_blocks) {   // the rows read as zeros
+        set_error(kErrBadBlock);
+        return -1;
+    }
     return ((int64_t)bid << a.block_size_log2) + (t & ((1 << a.block_size_log2) - 1));
 }
 
@@ -776,19 +777,7 @@ void set_prefill_fault(int mode) { g_fault_mode.store(mode); }
 int prefill_fault() { return g_fault_mode.load(); }
 
 cudaError_t take_prefill_error(cudaStream_t stream, int *code) {
-    int v = 0;
-    cudaError_t e = cudaMemcpyFromSymbolAsync(&v, g_prefill_error, sizeof(int), 0,
-                                              cudaMemcpyDeviceToHost, stream);
-    if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    if (e != cudaSuccess) return e;
-    *code = v;
-    if (v != 0) {
-        const int zero = 0;
-        e = cudaMemcpyToSymbolAsync(g_prefill_error, &zero, sizeof(int), 0,
-                                    cudaMemcpyHostToDevice, stream);
-        if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
-    }
-    return e;
+    return take_device_word(g_prefill_error, stream, code);
 }
 
 }  // namespace pa

@@ -11,6 +11,8 @@
 
 namespace pa {
 
+__device__ int g_store_error;        // first device-side error of a store launch
+
 namespace {
 
 constexpr int kStoreWarps = 8;
@@ -30,7 +32,10 @@ store_kvcache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
     const int64_t stride = (int64_t)gridDim.x * kStoreWarps;
     for (int64_t i = first; i < num_tokens; i += stride) {
         const int64_t slot = slot_mapping[i];
-        if (slot < 0 || slot >= num_slots) continue;   // -1 padding, or out of range
+        if (slot < 0 || slot >= num_slots) {          // -1 padding, or out of range
+            if (slot != -1 && lane == 0) atomicCAS(&g_store_error, 0, kErrBadSlot);
+            continue;
+        }
         const uint4 *ks = k + i * row_chunks;
         const uint4 *vs = v + i * row_chunks;
         for (int c = lane; c < row_chunks; c += 32) {
@@ -53,6 +58,10 @@ store_kvcache_kernel(const uint4 *__restrict__ k, const uint4 *__restrict__ v,
 }
 
 }  // namespace
+
+cudaError_t take_store_error(cudaStream_t stream, int *code) {
+    return take_device_word(g_store_error, stream, code);
+}
 
 cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
                                  const int64_t *slot_mapping, int64_t num_tokens,
