@@ -234,6 +234,14 @@ PA_API pa_status_t pa_decode_layout(const void *q, const void *k_cache, const vo
                                     int head_dim, int block_size, int64_t num_blocks,
                                     pa_layout_t layout, void *workspace, size_t workspace_bytes,
                                     int num_partitions, void *stream);
+/* pa_decode_multi for a pool in either layout (same workspace size). */
+PA_API pa_status_t pa_decode_multi_layout(const void *q, const void *k_cache, const void *v_cache,
+                                          const int32_t *block_tables, int max_blocks_per_seq,
+                                          const int32_t *context_lens, int q_len, float scale,
+                                          void *out, int num_seqs, int num_q_heads,
+                                          int num_kv_heads, int head_dim, int block_size,
+                                          int64_t num_blocks, pa_layout_t layout, void *workspace,
+                                          size_t workspace_bytes, void *stream);
 
 /*
  * Paged prefill (chunked prefill): a chunk of new tokens per sequence attends

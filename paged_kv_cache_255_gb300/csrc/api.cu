@@ -217,6 +217,17 @@ pa_status_t pa_decode_multi(const void *q, const void *k_cache, const void *v_ca
                        workspace_bytes, 0, stream);
 }
 
+pa_status_t pa_decode_multi_layout(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, int q_len, float scale, void *out,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int64_t num_blocks, pa_layout_t layout,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       q_len, scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       block_size, num_blocks, layout, workspace, workspace_bytes, 0, stream);
+}
+
 pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,
                        const int32_t *block_tables, int max_blocks_per_seq,
                        const int32_t *context_lens, const int32_t *query_start_loc,

@@ -44,6 +44,8 @@ SIGNATURES = {
                           _I32, _P, _SZ, _I32, _P], _I32),
     "pa_decode_multi": ([_P, _P, _P, _P, _I32, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                          _I64, _P, _SZ, _P], _I32),
+    "pa_decode_multi_layout": ([_P, _P, _P, _P, _I32, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32,
+                                _I32, _I64, _I32, _P, _SZ, _P], _I32),
 }
 
 _lock = threading.Lock()
@@ -204,17 +206,22 @@ def decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=None, wor
 
 
 def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out=None,
-                 workspace=None, stream=None):
+                 workspace=None, stream=None, head_major=False):
     """Decode of Q new tokens per sequence (speculative verification): q is
     bf16 [S, Q, Hq, D]; query token i attends to keys t <= L - Q + i, with
-    L = context_lens[s] counting all Q new tokens. Returns out [S, Q, Hq, D]."""
+    L = context_lens[s] counting all Q new tokens. The pool is
+    [NB, bs, Hkv, D], or [NB, Hkv, bs, D] with head_major=True. Returns out
+    [S, Q, Hq, D]."""
     dev = q.device
     for t, n, dt in ((q, "q", torch.bfloat16), (k_cache, "k_cache", torch.bfloat16),
                      (v_cache, "v_cache", torch.bfloat16), (block_tables, "block_tables", torch.int32),
                      (context_lens, "context_lens", torch.int32)):
         _cuda(t, n, dt, dev)
     S, Q, Hq, D = q.shape
-    NB, bs, Hkv, D2 = k_cache.shape
+    if head_major:
+        NB, Hkv, bs, D2 = k_cache.shape
+    else:
+        NB, bs, Hkv, D2 = k_cache.shape
     if v_cache.shape != k_cache.shape or D2 != D or block_tables.dim() != 2 \
             or block_tables.shape[0] != S or context_lens.shape != (S,):
         raise ValueError("shape mismatch between q, caches, block_tables and context_lens")
@@ -238,12 +245,13 @@ def decode_multi(q, k_cache, v_cache, block_tables, context_lens, scale, out=Non
         _cuda(workspace, "workspace", workspace.dtype, dev)
     ws_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
-        st = lib().pa_decode_multi(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
-                                   block_tables.data_ptr(), block_tables.shape[1],
-                                   context_lens.data_ptr(), Q, float(scale), out.data_ptr(), S,
-                                   Hq, Hkv, D, bs, NB, workspace.data_ptr(), ws_bytes,
-                                   _stream_ptr(stream, dev))
-    _check("pa_decode_multi", st)
+        st = lib().pa_decode_multi_layout(q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                          block_tables.data_ptr(), block_tables.shape[1],
+                                          context_lens.data_ptr(), Q, float(scale),
+                                          out.data_ptr(), S, Hq, Hkv, D, bs, NB,
+                                          1 if head_major else 0,
+                                          workspace.data_ptr(), ws_bytes, _stream_ptr(stream, dev))
+    _check("pa_decode_multi_layout", st)
     return out
 
 

@@ -2,8 +2,8 @@
 
 Each case draws the group size, the KV heads, the block size, the pool mode,
 a length mix with zero-length sequences and lengths on and next to block
-edges, the number of query tokens per sequence, and (for single-token steps)
-the pool layout and a forced partition count. The store is checked bit for
+edges, the number of query tokens per sequence, the pool layout, and (for
+single-token steps) a forced partition count. The store is checked bit for
 bit and every output element against the oracle.
 """
 import numpy as np
@@ -45,7 +45,7 @@ def _draw(case):
             lens.append(int(rng.integers(1, 1500)))
     spec = inputs.Spec(f"rand{case}", ((S, 1, 1),), g * hkv, hkv, bs,
                        pool_mode=str(rng.choice(["permute", "fragmented"])), pool_factor=1.3)
-    head_major = bool(rng.integers(0, 2)) and q_len == 1
+    head_major = bool(rng.integers(0, 2))
     parts = int(rng.choice([0, 0, 1, 3, 17, 300])) if q_len == 1 else 0
     return spec, np.asarray(lens, np.int32), q_len, head_major, parts
 
@@ -69,11 +69,13 @@ def test_random_decode_step(case):
         kc, vc = O.store_kvcache(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping)
         ref = O.decode_multi(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
         pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
-        out = pa.decode_multi(q.cuda(), d["k_cache"], d["v_cache"], d["block_tables"],
-                              d["context_lens"], wl.scale)
         torch.cuda.synchronize()
         assert np.array_equal(gu.host_bits(d["k_cache"]), kc), what
         assert np.array_equal(gu.host_bits(d["v_cache"]), vc), what
+        kd, vd = (_hm(d["k_cache"]), _hm(d["v_cache"])) if head_major else (d["k_cache"], d["v_cache"])
+        out = pa.decode_multi(q.cuda(), kd, vd, d["block_tables"], d["context_lens"], wl.scale,
+                              head_major=head_major)
+        torch.cuda.synchronize()
     elif head_major:
         hk_ref, hv_ref = O.store_kvcache_head_major(wl.k_new, wl.v_new, _hm(wl.k_cache),
                                                     _hm(wl.v_cache), wl.slot_mapping)

@@ -60,3 +60,32 @@ def test_head_major_store_and_decode(name):
 def test_layout_argument_is_checked(pa_lib):
     assert pa_lib.pa_store_kvcache_layout(16, 16, 16, 16, 16, 4, 8, 128, 16, 10, 7, None) == \
         pa.PA_ERR_INVALID_ARG
+
+
+@pytest.mark.parametrize("name,Q", [("tiny", 3), ("large_small", 4), ("bs256", 8)])
+def test_head_major_multi_token_decode(name, Q):
+    """pa_decode_multi_layout on a head-major pool: against the oracle, and bit
+    for bit against the token-major pool holding the same values."""
+    wl = inputs.generate(CASES[name], seed=63)
+    O = oracle.get()
+    q = torch.randn((wl.num_seqs, Q, wl.spec.num_q_heads, wl.spec.head_dim),
+                    generator=torch.Generator().manual_seed(64)).to(torch.bfloat16)
+    kc, vc = O.store_kvcache(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping)
+    ref = O.decode_multi(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+    d = gu.device_inputs(wl)
+    pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+    hk, hv = hm(d["k_cache"]), hm(d["v_cache"])
+    qd = q.cuda()
+    a = pa.decode_multi(qd, d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                        wl.scale)
+    b = pa.decode_multi(qd, hk, hv, d["block_tables"], d["context_lens"], wl.scale,
+                        head_major=True)
+    torch.cuda.synchronize()
+    gu.assert_close(b, ref, f"{name} Q={Q} head-major")
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_multi_layout_argument_is_checked(pa_lib):
+    st = pa_lib.pa_decode_multi_layout(None, None, None, None, 1, None, 2, 1.0, None, 1, 16, 8,
+                                       128, 16, 4, 7, None, 0, None)
+    assert st == 1    # PA_ERR_INVALID_ARG
