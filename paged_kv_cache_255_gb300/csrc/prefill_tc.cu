@@ -25,7 +25,8 @@
 //                    descriptors name, into 3 K stages and 2 V stages. V rows
 //                    of a partly used 16-token group at the end of the keys
 //                    are copied (rows past the end zeroed) by the lanes.
-//   warp 10          Q producer: both query tiles, by 16-byte cp.async.
+//   warp 10          Q producer: both query tiles, by TMA (a 3-D tensor map
+//                    over q: dims x heads x tokens).
 //   warp 11          issues the MMAs (converged warp, one elected lane):
 //                      S_t(j)  = Q_t K_j^T      M 128, N 128, K 16 x 8 (smem, smem)
 //                      O_t    += P_t(j) V_j     M 128, N 128, K 16 x 8 (TMEM, smem)
@@ -251,7 +252,8 @@ __device__ __forceinline__ Item make_item(int qp, int n, int L) {
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
-                  const __grid_constant__ CUtensorMap tmap_v) {
+                  const __grid_constant__ CUtensorMap tmap_v,
+                  const __grid_constant__ CUtensorMap tmap_q) {
     constexpr int BT = kRows / G;               // query tokens per query tile
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5;
@@ -528,7 +530,6 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
     } else if (warp == kQWarp) {
         // ---------------- Q producer ----------------
         const int lane = tid & 31;
-        const uint16_t *qg = static_cast<const uint16_t *>(a.q);
         int item = 0;
         bool ok = true;
 #pragma unroll 1
@@ -537,24 +538,20 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             if (item > 0 && !warp_wait(bar(kBarQEmpty), (item - 1) & 1, abort)) { ok = false; break; }
-            // Q_A and Q_B: row r of the pair is token tok0 + r / G, head r % G
-#pragma unroll 8
-            for (int i = 0; i < (2 * kRows * 16) / 32; ++i) {
-                const int c = lane + i * 32;
-                const int row = c >> 4, chunk = c & 15;
-                const int tok = it.tok0 + row / G, head = row % G;
-                const bool rv = tok < n && head < g;
-                const int rr = row & (kRows - 1);
-                const uint32_t dst = sbase + kOffQ + (row >> 7) * kQBytes + (chunk >> 3) * kQHalf +
-                                     rr * 128 + ((((uint32_t)chunk & 7) ^ ((uint32_t)rr & 7)) << 4);
-                const int64_t e = ((int64_t)q0 + tok) * a.num_q_heads + (int64_t)kvh * g + head;
-                cp_async_16(dst, rv ? reinterpret_cast<const char *>(qg + e * kHeadDim) + chunk * 16
-                                    : static_cast<const void *>(qg),
-                            rv ? 16 : 0);
+            // Q_A and Q_B: row r of tile t is token tok0 + t BT + r / G, head
+            // kvh g + r % G. One TMA box of 64 dims x G heads x BT tokens per
+            // tile half lands as those 128 rows of 128 B, 128-byte swizzled, as
+            // the S descriptors read them. Rows past the chunk or the group's
+            // heads hold other rows' values, or zeros past the tensor: each row
+            // of S, P and O depends on its own q row only, and those rows are
+            // never written out.
+            if (lane == 0) {
+                tc::mbar_expect_tx(bar(kBarQFull), 2 * kQBytes);
+                for (int t = 0; t < 2; ++t)
+                    for (int h = 0; h < 2; ++h)
+                        tc::tma_load_3d(sbase + kOffQ + t * kQBytes + h * kQHalf, &tmap_q, h * 64,
+                                        kvh * g, q0 + it.tok0 + t * BT, bar(kBarQFull));
             }
-            cp_async_commit();
-            cp_async_wait<0>();
-            tc::fence_proxy_async();
             warp_arrive(bar(kBarQFull));
         }
     } else if (warp == kMmaWarp) {
@@ -733,6 +730,21 @@ bool make_pool_map(CUtensorMap *m, const void *pool, int64_t num_blocks, int blo
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// q [total_q, Hq, 128] bf16 as a 3-D tensor (128, Hq, total_q) with boxes of
+// 64 dims x G heads x 128 / G tokens, 128-byte swizzle: one box is one half
+// (64 dims) of a 128-row query tile.
+bool make_q_map(CUtensorMap *m, const void *q, int total_q, int num_q_heads, int G) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
+    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)num_q_heads * kRowBytes};
+    const cuuint32_t box[3] = {64, (cuuint32_t)G, (cuuint32_t)(kRows / G)};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(q), dims, strides, box,
+               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 template <int G>
 cudaError_t launch_g(const PrefillArgs &a, int max_query_len, cudaStream_t st) {
     cudaError_t e = cudaFuncSetAttribute(prefill_tc_kernel<G>,
@@ -743,15 +755,16 @@ cudaError_t launch_g(const PrefillArgs &a, int max_query_len, cudaStream_t st) {
         a.num_blocks * a.num_kv_heads >= (int64_t)1 << 31)
         return cudaErrorInvalidValue;
     const int bs = 1 << a.block_size_log2;
-    CUtensorMap mk, mv;
+    CUtensorMap mk, mv, mq;
     if (!make_pool_map(&mk, a.k_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0) ||
-        !make_pool_map(&mv, a.v_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0))
+        !make_pool_map(&mv, a.v_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0) ||
+        !make_q_map(&mq, a.q, a.total_q, a.num_q_heads, G))
         return cudaErrorInvalidValue;
     constexpr int BT = kRows / G;
     const int pairs = (max_query_len + 2 * BT - 1) / (2 * BT);
     int gx = (pairs + kPairsPerCta - 1) / kPairsPerCta;
     gx = gx < 1 ? 1 : (gx > 65535 ? 65535 : gx);
-    prefill_tc_kernel<G><<<dim3(gx, a.num_seqs, a.num_kv_heads), kThreads, kSmemBytes, st>>>(a, mk, mv);
+    prefill_tc_kernel<G><<<dim3(gx, a.num_seqs, a.num_kv_heads), kThreads, kSmemBytes, st>>>(a, mk, mv, mq);
     return cudaGetLastError();
 }
 

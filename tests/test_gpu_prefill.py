@@ -38,6 +38,9 @@ CASES = [
      [0, 0, 16, 1, 65, 3]),
     # many short whole prompts: 300 sequences of 1..40 tokens (one CTA row per sequence)
     ("many_short", _spec("h", 16, 4, 16), None, _MANY, _MANY),
+    # one KV head with a group that pads up: the padded group is taller than q's heads
+    ("g3_one_kv", _spec("i", 3, 1, 16), None, [150, 40], [150, 17]),
+    ("g6_one_kv", _spec("j", 6, 1, 32), None, [90, 260], [90, 65]),
 ]
 
 
