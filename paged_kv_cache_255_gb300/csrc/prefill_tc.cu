@@ -98,8 +98,14 @@ constexpr uint32_t kBarOFree = kBarPVDone + 2;
 constexpr uint32_t kNumBars = kBarOFree + 2;
 constexpr uint32_t kOffTmemSlot = kOffCtl + 8 * kNumBars;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
-constexpr uint32_t kSmemBytes = kOffCtl + 256;
-static_assert(kOffAbort + 4 <= kSmemBytes, "control block");
+constexpr uint32_t kOffSeqSlot = kOffAbort + 4;
+// heavy-first sequence order (up to kRankMaxSeqs sequences): their lengths and
+// query starts, staged once per CTA
+constexpr int kRankMaxSeqs = 256;
+constexpr uint32_t kOffSeqLens = kOffCtl + 256;
+constexpr uint32_t kOffSeqStarts = kOffSeqLens + 4 * kRankMaxSeqs;
+constexpr uint32_t kSmemBytes = kOffSeqStarts + 4 * (kRankMaxSeqs + 1) + 12;
+static_assert(kOffSeqSlot + 4 <= kOffSeqLens, "control block");
 static_assert(kSmemBytes <= 232448, "shared memory");
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, kKeys, false);
@@ -257,11 +263,46 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
     constexpr int BT = kRows / G;               // query tokens per query tile
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int s = blockIdx.y, kvh = blockIdx.z;
+    const int kvh = blockIdx.z;
     const int g = a.group;
+    const int64_t max_len = (int64_t)a.max_blocks_per_seq << a.block_size_log2;
 
-    int q0 = __ldg(a.query_start_loc + s);
-    int q1 = __ldg(a.query_start_loc + s + 1);
+    // The sequence of this grid row. The block scheduler starts CTAs in grid
+    // order, so with few enough sequences row y takes the one of rank y by
+    // context length (longest first, ties by index): the longest work starts
+    // first and the last wave holds the shortest. Every CTA ranks the same
+    // staged lengths, so the rows map one to one onto the sequences.
+    int s = blockIdx.y, q0, q1, L;
+    if (a.num_seqs <= kRankMaxSeqs) {
+        int *lens = reinterpret_cast<int *>(smem + kOffSeqLens);
+        int *starts = reinterpret_cast<int *>(smem + kOffSeqStarts);
+        volatile int *slot = reinterpret_cast<volatile int *>(smem + kOffSeqSlot);
+        if (tid < a.num_seqs) {
+            const int64_t l = __ldg(a.context_lens + tid);
+            lens[tid] = (int)(l < 0 ? 0 : (l > max_len ? max_len : l));
+        }
+        if (tid <= a.num_seqs) starts[tid] = __ldg(a.query_start_loc + tid);
+        __syncthreads();
+        if (tid < a.num_seqs) {
+            const int lj = lens[tid];
+            int rank = 0;
+            for (int i = 0; i < a.num_seqs; ++i) {
+                const int li = lens[i];
+                rank += (li > lj || (li == lj && i < tid)) ? 1 : 0;
+            }
+            if (rank == (int)blockIdx.y) *slot = tid;
+        }
+        __syncthreads();
+        s = *slot;
+        q0 = starts[s];
+        q1 = starts[s + 1];
+        L = lens[s];
+    } else {
+        q0 = __ldg(a.query_start_loc + s);
+        q1 = __ldg(a.query_start_loc + s + 1);
+        const int64_t l = __ldg(a.context_lens + s);
+        L = (int)(l < 0 ? 0 : (l > max_len ? max_len : l));
+    }
     q0 = q0 < 0 ? 0 : (q0 > a.total_q ? a.total_q : q0);
     q1 = q1 < q0 ? q0 : (q1 > a.total_q ? a.total_q : q1);
     const int n = q1 - q0;
@@ -272,11 +313,6 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
     if (sbase & 1023u) {                        // the swizzle atoms need 1024-byte alignment
         if (tid == 0) set_error(kErrSmemAlign);
         return;
-    }
-    int L = __ldg(a.context_lens + s);
-    {
-        const int64_t max_len = (int64_t)a.max_blocks_per_seq << a.block_size_log2;
-        L = L < 0 ? 0 : ((int64_t)L > max_len ? (int)max_len : L);
     }
 
     const uint32_t ctl = sbase + kOffCtl;
