@@ -1,6 +1,6 @@
 /*
- * libpagedattn -- paged KV-cache store and single-token decode attention,
- * for NVIDIA GB300 (sm_103a).
+ * libpagedattn -- paged KV-cache store, decode attention (one or several new
+ * tokens per sequence) and paged prefill attention, for NVIDIA GB300 (sm_103a).
  *
  * The operations follow the pages that describe a minimal vLLM engine:
  *   - KV is kept in fixed-size token blocks of one pool
@@ -25,7 +25,10 @@
  *   context_lens [num_seqs] int32, tokens of each sequence, counting the one
  *                just stored
  *   out          [num_seqs, num_q_heads, head_dim]                 bf16
- * Query head h reads KV head h / (num_q_heads / num_kv_heads).
+ * Query head h reads KV head h / (num_q_heads / num_kv_heads). The *_layout
+ * calls also take the head-major pool [num_blocks, num_kv_heads, block_size,
+ * head_dim]; pa_decode_multi and pa_prefill take their q and out shapes as
+ * described at each call.
  *
  * Ownership: every pointer is caller-owned memory on the current CUDA device
  * (the workspace included). The library allocates nothing and keeps no state
@@ -36,9 +39,10 @@
  * launched, and returned as a status. Index values the kernels read on the
  * device (slots, block ids, lengths) are never trusted for addressing: a slot
  * outside [-1, num_blocks * block_size) writes nothing, a block id outside
- * [0, num_blocks) contributes no tokens, a length is clamped to
- * [0, max_blocks_per_seq * block_size]. Such inputs give unspecified output
- * values but never touch memory outside the buffers passed in.
+ * [0, num_blocks) reads as zero rows (keys that score 0 and add a zero value),
+ * a length is clamped to [0, max_blocks_per_seq * block_size]. Such inputs
+ * never touch memory outside the buffers passed in, and the first two are
+ * recorded on the device for pa_take_device_error.
  */
 #ifndef PAGEDATTN_H
 #define PAGEDATTN_H
