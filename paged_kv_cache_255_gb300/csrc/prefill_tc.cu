@@ -230,7 +230,8 @@ __device__ __forceinline__ int groups_full(int k0, int kend) {
 struct Item {
     int tok0;       // first token of tile A
     int kend;       // keys the pair reads: L - n + (its last token) + 1
-    int nt;         // K/V tiles
+    int nt;         // K/V tiles (the more of the two query tiles' counts)
+    int nta, ntb;   // key tiles query tile A, B reads (B: 0 when the chunk ends in A)
 };
 
 // Pair index of the i-th item of CTA b of the g CTAs of a (sequence, KV
@@ -252,6 +253,13 @@ __device__ __forceinline__ Item make_item(int qp, int n, int L) {
     int kend = L - n + last_tok + 1;
     it.kend = kend < 0 ? 0 : (kend > L ? L : kend);
     it.nt = (it.kend + kKeys - 1) / kKeys;
+    // tile A's own last token may need one key tile fewer; tile B holds tokens
+    // only if the chunk reaches past tile A
+    const int last_a = (it.tok0 + BT < n ? it.tok0 + BT : n) - 1;
+    int kend_a = L - n + last_a + 1;
+    kend_a = kend_a < 0 ? 0 : (kend_a > L ? L : kend_a);
+    it.nta = (kend_a + kKeys - 1) / kKeys;
+    it.ntb = it.tok0 + BT < n ? it.nt : 0;
     return it;
 }
 
@@ -353,7 +361,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         // a masked score for the max: the value that loses whatever the
         // scale's sign (masked keys then get p = 0 directly)
         const float masked = sc >= 0.f ? -INFINITY : INFINITY;
-        uint32_t gt = 0;                        // tiles done before this item
+        uint32_t gt = 0;                        // this query tile's key tiles before this item
         bool ok = true;
 #pragma unroll 1
         for (int i = 0; ok; ++i) {
@@ -367,9 +375,10 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 const int l = L - n + tok + 1;
                 lim = l < 0 ? 0 : (l > L ? L : l);
             }
+            const int ntt = wg == 0 ? it.nta : it.ntb;  // key tiles this query tile reads
             float m = -INFINITY, lsum = 0.f;
 #pragma unroll 1
-            for (int j = 0; j < it.nt; ++j) {
+            for (int j = 0; j < ntt; ++j) {
                 const uint32_t gj = gt + j;
                 // S_t(j) done: also PV_t(j - 1) (issued before it), so O is stable
                 if (!warp_wait(bar(kBarSFull + wg), gj & 1, abort, true)) { ok = false; break; }
@@ -467,8 +476,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             }
             if (!ok) break;
             // epilogue: O / l -> bf16 rows; then O is free for the next item
-            if (it.nt > 0) {
-                if (!warp_wait(bar(kBarPVDone + wg), (gt + it.nt - 1) & 1, abort, true)) { ok = false; break; }
+            if (ntt > 0) {
+                if (!warp_wait(bar(kBarPVDone + wg), (gt + ntt - 1) & 1, abort, true)) { ok = false; break; }
                 tc::fence_after_sync();
             }
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
@@ -477,7 +486,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
                 uint32_t o[32];
-                if (it.nt > 0) {
+                if (ntt > 0) {
                     tc::tmem_ld32(tO + ch * 32, o);
                     tc::tmem_ld_wait();
                 } else {
@@ -498,7 +507,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             }
             tc::fence_before_sync();
             warp_arrive(bar(kBarOFree + wg));
-            gt += it.nt;
+            gt += ntt;
         }
     } else if (warp == kKWarp || warp == kVWarp) {
         // ---------------- K and V producers ----------------
@@ -652,7 +661,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         // TMEM and V_y has landed (and, for the first PV of an item, the
         // previous item's O has been read). A K stage is released after the
         // second S that reads it, a V stage after the second PV.
-        uint32_t gt = 0;
+        uint32_t gt = 0;                        // the pair's key tiles before this item (K/V stages)
+        uint32_t gq0 = 0, gq1 = 0;              // each query tile's key tiles before this item
         int item = 0;
         bool ok = true;
 #pragma unroll 1
@@ -665,7 +675,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             uint64_t t_idle = 0;
             uint32_t idle = 0;
 #pragma unroll 1
-            while (ok && (pj0 < it.nt || pj1 < it.nt)) {
+            while (ok && (pj0 < it.nta || pj1 < it.ntb)) {
                 bool progress = false;
 #pragma unroll
                 for (int t = 0; t < 2; ++t) {
@@ -673,24 +683,28 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                     int &pj = t == 0 ? pj0 : pj1;
                     const int other_pj = t == 0 ? pj1 : pj0;
                     const int other_sj = t == 0 ? sj1 : sj0;
+                    const int my_nt = t == 0 ? it.nta : it.ntb;
+                    const int other_nt = t == 0 ? it.ntb : it.nta;
+                    const uint32_t my_gq = t == 0 ? gq0 : gq1;
                     if (pj < sj) {
                         const uint32_t gp = gt + pj;
                         const int st = gp % kVStages;
-                        bool go = ready(bar(kBarPReady + t), gp & 1) &&
+                        bool go = ready(bar(kBarPReady + t), (my_gq + pj) & 1) &&
                                   ready(bar(kBarVFull + st), (gp / kVStages) & 1);
                         if (go && pj == 0 && item > 0) go = ready(bar(kBarOFree + t), (item - 1) & 1);
                         if (go) {
+                            // the V stage is released by its last reader
                             issue_pv(t, st, pj > 0, groups_used(pj * kKeys, it.kend),
-                                     other_pj > pj ? bar(kBarVEmpty + st) : 0u);
+                                     other_pj > pj || other_nt <= pj ? bar(kBarVEmpty + st) : 0u);
                             ++pj;
                             progress = true;
                         }
                     }
-                    if (sj == pj && sj < it.nt) {
+                    if (sj == pj && sj < my_nt) {
                         const uint32_t gs = gt + sj;
                         const int st = gs % kKStages;
                         if (ready(bar(kBarKFull + st), (gs / kKStages) & 1)) {
-                            issue_s(t, st, other_sj > sj ? bar(kBarKEmpty + st) : 0u);
+                            issue_s(t, st, other_sj > sj || other_nt <= sj ? bar(kBarKEmpty + st) : 0u);
                             ++sj;
                             progress = true;
                         }
@@ -721,6 +735,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             if (tc::elect_one()) tc::commit(bar(kBarQEmpty));
             __syncwarp();
             gt += it.nt;
+            gq0 += it.nta;
+            gq1 += it.ntb;
         }
     }
 
