@@ -659,8 +659,10 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         // Event-driven issue for each query tile t: S_t(x) once K_x has
         // landed and PV_t(x - 1) has been issued; PV_t(y) once P_t(y) is in
         // TMEM and V_y has landed (and, for the first PV of an item, the
-        // previous item's O has been read). A K stage is released after the
-        // second S that reads it, a V stage after the second PV.
+        // previous item's O has been read), each tile up to its own count of
+        // key tiles. A K stage is released after the last S that reads it
+        // (the second, or the only one when the other tile stops short), a V
+        // stage after the last PV.
         uint32_t gt = 0;                        // the pair's key tiles before this item (K/V stages)
         uint32_t gq0 = 0, gq1 = 0;              // each query tile's key tiles before this item
         int item = 0;
