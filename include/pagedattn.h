@@ -35,6 +35,13 @@
  * between calls. Calls are asynchronous on `stream` (a cudaStream_t; NULL is
  * the legacy default stream) and return once the kernels are queued.
  *
+ * Tracing: every call that launches work (and pa_take_device_error) opens one
+ * NVTX range named after itself, in the NVTX domain "libpagedattn", for as
+ * long as it runs on the host; the kernels it queues carry that range in
+ * Nsight tools (e.g. `ncu --nvtx --nvtx-include "libpagedattn@pa_decode/"`).
+ * pa_decode_noalloc shows as pa_decode. With no tool attached a range costs a
+ * test of a function pointer.
+ *
  * Errors: argument problems are found on the host, before anything is
  * launched, and returned as a status. Index values the kernels read on the
  * device (slots, block ids, lengths) are never trusted for addressing: a slot

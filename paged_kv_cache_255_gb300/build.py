@@ -67,7 +67,7 @@ def build(force: bool = False, verbose: bool = False, extra_flags=()) -> str:
     if failed:
         raise RuntimeError("nvcc failed:\n" + "\n".join(f"{s}:\n{o}" for s, o in failed))
     tmp = LIB_PATH + f".tmp{os.getpid()}"
-    subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs], check=True)
+    subprocess.run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-ldl"], check=True)   # -ldl: NVTX loads a tool by dlopen
     os.replace(tmp, LIB_PATH)
     return LIB_PATH
 

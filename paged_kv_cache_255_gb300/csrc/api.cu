@@ -5,10 +5,36 @@
 #include <cstdlib>
 #include <cstring>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/pagedattn.h"
 #include "kernels.h"
 
 namespace {
+
+// One NVTX range per public call, named after the entry point, in the domain
+// "libpagedattn": a timeline, or an Nsight Compute run filtered with --nvtx,
+// shows which call launched each kernel. With no tool attached a push or a pop
+// is a test of a function pointer.
+nvtxDomainHandle_t trace_domain() {
+    static const nvtxDomainHandle_t d = nvtxDomainCreateA("libpagedattn");
+    return d;
+}
+
+class TraceRange {
+  public:
+    explicit TraceRange(const char *name) {
+        nvtxEventAttributes_t a{};
+        a.version = NVTX_VERSION;
+        a.size = NVTX_EVENT_ATTRIB_STRUCT_SIZE;
+        a.messageType = NVTX_MESSAGE_TYPE_ASCII;
+        a.message.ascii = name;
+        nvtxDomainRangePushEx(trace_domain(), &a);
+    }
+    ~TraceRange() { nvtxDomainRangePop(trace_domain()); }
+    TraceRange(const TraceRange &) = delete;
+    TraceRange &operator=(const TraceRange &) = delete;
+};
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -98,25 +124,10 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-}  // namespace
-
-extern "C" {
-
-const char *pa_status_string(pa_status_t status) {
-    switch (status) {
-        case PA_OK: return "PA_OK";
-        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
-        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
-        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
-        case PA_ERR_CUDA: return "PA_ERR_CUDA";
-    }
-    return "PA_ERR_UNKNOWN";
-}
-
-pa_status_t pa_store_kvcache_layout(const void *k, const void *v, void *k_cache, void *v_cache,
-                                    const int64_t *slot_mapping, int64_t num_tokens,
-                                    int num_kv_heads, int head_dim, int block_size,
-                                    int64_t num_blocks, pa_layout_t layout, void *stream) {
+pa_status_t store_impl(const void *k, const void *v, void *k_cache, void *v_cache,
+                       const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                       int head_dim, int block_size, int64_t num_blocks, int layout,
+                       void *stream) {
     if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
     if (layout != PA_LAYOUT_TOKEN_MAJOR && layout != PA_LAYOUT_HEAD_MAJOR) return PA_ERR_INVALID_ARG;
     if (head_dim != pa::kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
@@ -133,120 +144,12 @@ pa_status_t pa_store_kvcache_layout(const void *k, const void *v, void *k_cache,
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
-pa_status_t pa_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
-                             const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
-                             int head_dim, int block_size, int64_t num_blocks, void *stream) {
-    return pa_store_kvcache_layout(k, v, k_cache, v_cache, slot_mapping, num_tokens,
-                                   num_kv_heads, head_dim, block_size, num_blocks,
-                                   PA_LAYOUT_TOKEN_MAJOR, stream);
-}
-
-size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
-                                int num_partitions) {
-    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
-        head_dim != pa::kHeadDimPublic || num_partitions < 0)
-        return 0;
-    const int gp = pa::decode_group_pad(num_q_heads / num_kv_heads);
-    if (gp == 0) return 0;
-    // sized for the larger of the two variants' default share counts
-    int P = plan_workers(gp, pa::DecodeKernel::kMma, num_partitions);
-    if (num_partitions == 0 && gp <= 8) {
-        const int Ps = plan_workers(gp, pa::DecodeKernel::kSimt, 0);
-        P = Ps > P ? Ps : P;
-    }
-    if (P <= 0) return 0;
-    return pa::decode_workspace_bytes(gp, P);
-}
-
-pa_status_t pa_decode(const void *q, const void *k_cache, const void *v_cache,
-                      const int32_t *block_tables, int max_blocks_per_seq,
-                      const int32_t *context_lens, float scale, void *out, int num_seqs,
-                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                      int64_t num_blocks, void *workspace, size_t workspace_bytes,
-                      void *stream) {
-    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
-                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       num_blocks, PA_LAYOUT_TOKEN_MAJOR, workspace, workspace_bytes, 0, stream);
-}
-
-pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const void *v_cache,
-                             const int32_t *block_tables, int max_blocks_per_seq,
-                             const int32_t *context_lens, float scale, void *out, int num_seqs,
-                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                             int64_t num_blocks, void *workspace, size_t workspace_bytes,
-                             int num_partitions, void *stream) {
-    if (num_partitions < 0) return PA_ERR_INVALID_ARG;
-    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
-                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       num_blocks, PA_LAYOUT_TOKEN_MAJOR, workspace, workspace_bytes,
-                       num_partitions, stream);
-}
-
-size_t pa_decode_multi_workspace_size(int q_len, int num_q_heads, int num_kv_heads,
-                                      int head_dim) {
-    if (q_len < 1 || q_len > 16 || num_q_heads <= 0 || num_kv_heads <= 0 ||
-        num_q_heads % num_kv_heads != 0 || head_dim != pa::kHeadDimPublic)
-        return 0;
-    const int gp = pa::decode_group_pad(num_q_heads / num_kv_heads * q_len);
-    if (gp == 0) return 0;
-    const int P = plan_workers(gp, pa::DecodeKernel::kMma, 0);
-    return P > 0 ? pa::decode_workspace_bytes(gp, P) : 0;
-}
-
-pa_status_t pa_decode_layout(const void *q, const void *k_cache, const void *v_cache,
-                             const int32_t *block_tables, int max_blocks_per_seq,
-                             const int32_t *context_lens, float scale, void *out, int num_seqs,
-                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                             int64_t num_blocks, pa_layout_t layout, void *workspace,
-                             size_t workspace_bytes, int num_partitions, void *stream) {
-    if (num_partitions < 0) return PA_ERR_INVALID_ARG;
-    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
-                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                       num_blocks, layout, workspace, workspace_bytes, num_partitions, stream);
-}
-
-pa_status_t pa_decode_multi(const void *q, const void *k_cache, const void *v_cache,
-                            const int32_t *block_tables, int max_blocks_per_seq,
-                            const int32_t *context_lens, int q_len, float scale, void *out,
-                            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                            int block_size, int64_t num_blocks, void *workspace,
-                            size_t workspace_bytes, void *stream) {
-    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                       q_len, scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                       block_size, num_blocks, PA_LAYOUT_TOKEN_MAJOR, workspace,
-                       workspace_bytes, 0, stream);
-}
-
-pa_status_t pa_decode_multi_layout(const void *q, const void *k_cache, const void *v_cache,
-                                   const int32_t *block_tables, int max_blocks_per_seq,
-                                   const int32_t *context_lens, int q_len, float scale, void *out,
-                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
-                                   int block_size, int64_t num_blocks, pa_layout_t layout,
-                                   void *workspace, size_t workspace_bytes, void *stream) {
-    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                       q_len, scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                       block_size, num_blocks, layout, workspace, workspace_bytes, 0, stream);
-}
-
-pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,
-                       const int32_t *block_tables, int max_blocks_per_seq,
-                       const int32_t *context_lens, const int32_t *query_start_loc,
-                       int max_query_len, float scale, void *out, int num_seqs, int total_q,
-                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
-                       int64_t num_blocks, void *stream) {
-    return pa_prefill_layout(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                             query_start_loc, max_query_len, scale, out, num_seqs, total_q,
-                             num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                             PA_LAYOUT_TOKEN_MAJOR, stream);
-}
-
-pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const void *v_cache,
-                              const int32_t *block_tables, int max_blocks_per_seq,
-                              const int32_t *context_lens, const int32_t *query_start_loc,
-                              int max_query_len, float scale, void *out, int num_seqs,
-                              int total_q, int num_q_heads, int num_kv_heads, int head_dim,
-                              int block_size, int64_t num_blocks, pa_layout_t layout,
-                              void *stream) {
+pa_status_t prefill_impl(const void *q, const void *k_cache, const void *v_cache,
+                         const int32_t *block_tables, int max_blocks_per_seq,
+                         const int32_t *context_lens, const int32_t *query_start_loc,
+                         int max_query_len, float scale, void *out, int num_seqs, int total_q,
+                         int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                         int64_t num_blocks, int layout, void *stream) {
     if (layout != PA_LAYOUT_TOKEN_MAJOR && layout != PA_LAYOUT_HEAD_MAJOR) return PA_ERR_INVALID_ARG;
     if (num_seqs < 0 || total_q < 0 || num_q_heads <= 0 || num_kv_heads <= 0 ||
         num_blocks < 0 || max_blocks_per_seq < 0 || max_query_len < 0 || !std::isfinite(scale))
@@ -290,6 +193,157 @@ pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const void *v_
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
+}  // namespace
+
+extern "C" {
+
+const char *pa_status_string(pa_status_t status) {
+    switch (status) {
+        case PA_OK: return "PA_OK";
+        case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+        case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+        case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+        case PA_ERR_CUDA: return "PA_ERR_CUDA";
+    }
+    return "PA_ERR_UNKNOWN";
+}
+
+pa_status_t pa_store_kvcache_layout(const void *k, const void *v, void *k_cache, void *v_cache,
+                                    const int64_t *slot_mapping, int64_t num_tokens,
+                                    int num_kv_heads, int head_dim, int block_size,
+                                    int64_t num_blocks, pa_layout_t layout, void *stream) {
+    TraceRange r("pa_store_kvcache_layout");
+    return store_impl(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                      block_size, num_blocks, layout, stream);
+}
+
+pa_status_t pa_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
+                             const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
+                             int head_dim, int block_size, int64_t num_blocks, void *stream) {
+    TraceRange r("pa_store_kvcache");
+    return store_impl(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                      block_size, num_blocks, PA_LAYOUT_TOKEN_MAJOR, stream);
+}
+
+size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int head_dim,
+                                int num_partitions) {
+    if (num_q_heads <= 0 || num_kv_heads <= 0 || num_q_heads % num_kv_heads != 0 ||
+        head_dim != pa::kHeadDimPublic || num_partitions < 0)
+        return 0;
+    const int gp = pa::decode_group_pad(num_q_heads / num_kv_heads);
+    if (gp == 0) return 0;
+    // sized for the larger of the two variants' default share counts
+    int P = plan_workers(gp, pa::DecodeKernel::kMma, num_partitions);
+    if (num_partitions == 0 && gp <= 8) {
+        const int Ps = plan_workers(gp, pa::DecodeKernel::kSimt, 0);
+        P = Ps > P ? Ps : P;
+    }
+    if (P <= 0) return 0;
+    return pa::decode_workspace_bytes(gp, P);
+}
+
+pa_status_t pa_decode(const void *q, const void *k_cache, const void *v_cache,
+                      const int32_t *block_tables, int max_blocks_per_seq,
+                      const int32_t *context_lens, float scale, void *out, int num_seqs,
+                      int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                      int64_t num_blocks, void *workspace, size_t workspace_bytes,
+                      void *stream) {
+    TraceRange r("pa_decode");
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
+                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, PA_LAYOUT_TOKEN_MAJOR, workspace, workspace_bytes, 0, stream);
+}
+
+pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, float scale, void *out, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks, void *workspace, size_t workspace_bytes,
+                             int num_partitions, void *stream) {
+    TraceRange r("pa_decode_splitk");
+    if (num_partitions < 0) return PA_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
+                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, PA_LAYOUT_TOKEN_MAJOR, workspace, workspace_bytes,
+                       num_partitions, stream);
+}
+
+size_t pa_decode_multi_workspace_size(int q_len, int num_q_heads, int num_kv_heads,
+                                      int head_dim) {
+    if (q_len < 1 || q_len > 16 || num_q_heads <= 0 || num_kv_heads <= 0 ||
+        num_q_heads % num_kv_heads != 0 || head_dim != pa::kHeadDimPublic)
+        return 0;
+    const int gp = pa::decode_group_pad(num_q_heads / num_kv_heads * q_len);
+    if (gp == 0) return 0;
+    const int P = plan_workers(gp, pa::DecodeKernel::kMma, 0);
+    return P > 0 ? pa::decode_workspace_bytes(gp, P) : 0;
+}
+
+pa_status_t pa_decode_layout(const void *q, const void *k_cache, const void *v_cache,
+                             const int32_t *block_tables, int max_blocks_per_seq,
+                             const int32_t *context_lens, float scale, void *out, int num_seqs,
+                             int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                             int64_t num_blocks, pa_layout_t layout, void *workspace,
+                             size_t workspace_bytes, int num_partitions, void *stream) {
+    TraceRange r("pa_decode_layout");
+    if (num_partitions < 0) return PA_ERR_INVALID_ARG;
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
+                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, layout, workspace, workspace_bytes, num_partitions, stream);
+}
+
+pa_status_t pa_decode_multi(const void *q, const void *k_cache, const void *v_cache,
+                            const int32_t *block_tables, int max_blocks_per_seq,
+                            const int32_t *context_lens, int q_len, float scale, void *out,
+                            int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                            int block_size, int64_t num_blocks, void *workspace,
+                            size_t workspace_bytes, void *stream) {
+    TraceRange r("pa_decode_multi");
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       q_len, scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       block_size, num_blocks, PA_LAYOUT_TOKEN_MAJOR, workspace,
+                       workspace_bytes, 0, stream);
+}
+
+pa_status_t pa_decode_multi_layout(const void *q, const void *k_cache, const void *v_cache,
+                                   const int32_t *block_tables, int max_blocks_per_seq,
+                                   const int32_t *context_lens, int q_len, float scale, void *out,
+                                   int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
+                                   int block_size, int64_t num_blocks, pa_layout_t layout,
+                                   void *workspace, size_t workspace_bytes, void *stream) {
+    TraceRange r("pa_decode_multi_layout");
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                       q_len, scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                       block_size, num_blocks, layout, workspace, workspace_bytes, 0, stream);
+}
+
+pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,
+                       const int32_t *block_tables, int max_blocks_per_seq,
+                       const int32_t *context_lens, const int32_t *query_start_loc,
+                       int max_query_len, float scale, void *out, int num_seqs, int total_q,
+                       int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                       int64_t num_blocks, void *stream) {
+    TraceRange r("pa_prefill");
+    return prefill_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        query_start_loc, max_query_len, scale, out, num_seqs, total_q,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                        PA_LAYOUT_TOKEN_MAJOR, stream);
+}
+
+pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, const int32_t *query_start_loc,
+                              int max_query_len, float scale, void *out, int num_seqs,
+                              int total_q, int num_q_heads, int num_kv_heads, int head_dim,
+                              int block_size, int64_t num_blocks, pa_layout_t layout,
+                              void *stream) {
+    TraceRange r("pa_prefill_layout");
+    return prefill_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                        query_start_loc, max_query_len, scale, out, num_seqs, total_q,
+                        num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, layout,
+                        stream);
+}
+
 pa_status_t pa_debug_prefill_fault(int mode) {
     if (mode != 0 && mode != 1) return PA_ERR_INVALID_ARG;
     pa::set_prefill_fault(mode);
@@ -297,6 +351,7 @@ pa_status_t pa_debug_prefill_fault(int mode) {
 }
 
 pa_status_t pa_take_device_error(int32_t *code, void *stream) {
+    TraceRange r("pa_take_device_error");
     if (!code) return PA_ERR_INVALID_ARG;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     cudaError_t (*const take[])(cudaStream_t, int *) = {
