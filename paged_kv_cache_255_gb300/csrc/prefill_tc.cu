@@ -271,16 +271,18 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
     constexpr int BT = kRows / G;               // query tokens per query tile
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int kvh = blockIdx.z;
+    const int kvh = blockIdx.x;
     const int g = a.group;
     const int64_t max_len = (int64_t)a.max_blocks_per_seq << a.block_size_log2;
 
-    // The sequence of this grid row. The block scheduler starts CTAs in grid
-    // order, so with few enough sequences row y takes the one of rank y by
-    // context length (longest first, ties by index): the longest work starts
-    // first and the last wave holds the shortest. Every CTA ranks the same
-    // staged lengths, so the rows map one to one onto the sequences.
-    int s = blockIdx.y, q0, q1, L;
+    // Grid (KV head x, pair slot y, sequence z). The block scheduler starts
+    // CTAs in grid order (x fastest, z slowest), so with few enough sequences
+    // slice z takes the one of rank z by context length (longest first, ties
+    // by index), every KV head of its heaviest pair first: the longest work
+    // of the whole launch starts first and the last wave holds the shortest.
+    // Every CTA ranks the same staged lengths, so the slices map one to one
+    // onto the sequences.
+    int s = blockIdx.z, q0, q1, L;
     if (a.num_seqs <= kRankMaxSeqs) {
         int *lens = reinterpret_cast<int *>(smem + kOffSeqLens);
         int *starts = reinterpret_cast<int *>(smem + kOffSeqStarts);
@@ -298,7 +300,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 const int li = lens[i];
                 rank += (li > lj || (li == lj && i < tid)) ? 1 : 0;
             }
-            if (rank == (int)blockIdx.y) *slot = tid;
+            if (rank == (int)blockIdx.z) *slot = tid;
         }
         __syncthreads();
         s = *slot;
@@ -315,7 +317,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
     q1 = q1 < q0 ? q0 : (q1 > a.total_q ? a.total_q : q1);
     const int n = q1 - q0;
     const int np = (n + 2 * BT - 1) / (2 * BT);            // query-tile pairs of the chunk
-    if (pair_of(0, blockIdx.x, gridDim.x, np) < 0) return;
+    if (pair_of(0, blockIdx.y, gridDim.y, np) < 0) return;
 
     const uint32_t sbase = smem_u32(smem);
     if (sbase & 1023u) {                        // the swizzle atoms need 1024-byte alignment
@@ -365,7 +367,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         bool ok = true;
 #pragma unroll 1
         for (int i = 0; ok; ++i) {
-            const int qp = pair_of(i, blockIdx.x, gridDim.x, np);
+            const int qp = pair_of(i, blockIdx.y, gridDim.y, np);
             if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             const int tok = it.tok0 + wg * BT + r / G, head = r % G;
@@ -528,7 +530,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         bool ok = true;
 #pragma unroll 1
         for (int i = 0; ok; ++i) {
-            const int qp = pair_of(i, blockIdx.x, gridDim.x, np);
+            const int qp = pair_of(i, blockIdx.y, gridDim.y, np);
             if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             const int kend = it.kend;
@@ -579,7 +581,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         bool ok = true;
 #pragma unroll 1
         for (int i = 0; ok; ++i, ++item) {
-            const int qp = pair_of(i, blockIdx.x, gridDim.x, np);
+            const int qp = pair_of(i, blockIdx.y, gridDim.y, np);
             if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             if (item > 0 && !warp_wait(bar(kBarQEmpty), (item - 1) & 1, abort)) { ok = false; break; }
@@ -669,7 +671,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         bool ok = true;
 #pragma unroll 1
         for (int i = 0; ok; ++i, ++item) {
-            const int qp = pair_of(i, blockIdx.x, gridDim.x, np);
+            const int qp = pair_of(i, blockIdx.y, gridDim.y, np);
             if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             ok = warp_wait(bar(kBarQFull), item & 1, abort);
@@ -816,9 +818,9 @@ cudaError_t launch_g(const PrefillArgs &a, int max_query_len, cudaStream_t st) {
         return cudaErrorInvalidValue;
     constexpr int BT = kRows / G;
     const int pairs = (max_query_len + 2 * BT - 1) / (2 * BT);
-    int gx = (pairs + kPairsPerCta - 1) / kPairsPerCta;
-    gx = gx < 1 ? 1 : (gx > 65535 ? 65535 : gx);
-    prefill_tc_kernel<G><<<dim3(gx, a.num_seqs, a.num_kv_heads), kThreads, kSmemBytes, st>>>(a, mk, mv, mq);
+    int gy = (pairs + kPairsPerCta - 1) / kPairsPerCta;   // pair slots per (sequence, KV head)
+    gy = gy < 1 ? 1 : (gy > 65535 ? 65535 : gy);
+    prefill_tc_kernel<G><<<dim3(a.num_kv_heads, gy, a.num_seqs), kThreads, kSmemBytes, st>>>(a, mk, mv, mq);
     return cudaGetLastError();
 }
 
