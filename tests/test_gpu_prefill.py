@@ -22,6 +22,13 @@ def _spec(name, Hq, Hkv, bs):
 
 
 _MANY = [int(x) for x in np.random.default_rng(5).integers(1, 41, 300)]
+# the largest batch whose CTAs start longest-first (256 sequences are ranked in
+# shared memory; some chunks and one context empty); many_short (300) is past it
+_rng = np.random.default_rng(6)
+_CTX256 = [int(x) for x in _rng.integers(0, 300, 256)]
+_CHK256 = [0 if i % 17 == 3 else int(min(c, x))
+           for i, (c, x) in enumerate(zip(_CTX256, _rng.integers(1, 140, 256)))]
+_CTX256[20] = _CHK256[20] = 0
 
 # (id, spec, chunk, context_lens, chunk_lens)
 CASES = [
@@ -38,6 +45,7 @@ CASES = [
      [0, 0, 16, 1, 65, 3]),
     # many short whole prompts: 300 sequences of 1..40 tokens (one CTA row per sequence)
     ("many_short", _spec("h", 16, 4, 16), None, _MANY, _MANY),
+    ("ranked_256", _spec("p", 16, 4, 16), None, _CTX256, _CHK256),
     # one KV head with a group that pads up: the padded group is taller than q's heads
     ("g3_one_kv", _spec("i", 3, 1, 16), None, [150, 40], [150, 17]),
     ("g6_one_kv", _spec("j", 6, 1, 32), None, [90, 260], [90, 65]),
