@@ -31,9 +31,11 @@
  * described at each call.
  *
  * Ownership: every pointer is caller-owned memory on the current CUDA device
- * (the workspace included). The library allocates nothing and keeps no state
- * between calls. Calls are asynchronous on `stream` (a cudaStream_t; NULL is
- * the legacy default stream) and return once the kernels are queued.
+ * (the workspace included). The library allocates nothing and keeps no data
+ * between calls; its only process-wide state is the NVTX domain handle (see
+ * Tracing) and the static scratch of pa_decode_noalloc. Calls are
+ * asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
+ * stream) and return once the kernels are queued.
  *
  * Tracing: every call that launches work (and pa_take_device_error) opens one
  * NVTX range named after itself, in the NVTX domain "libpagedattn", for as
