@@ -37,6 +37,14 @@ MUTANTS = [
      "const int cap = context_lens[s] - n + i;"),
     ("store_skips_first_row", "if (slot == -1)\n            continue;",
      "if (slot == -1 || i == 0)\n            continue;"),
+    ("pv_reads_keys",
+     ": v_cache + ((block * block_size + t % block_size) * num_kv_heads + kvh) * (int64_t)head_dim;",
+     ": k_cache + ((block * block_size + t % block_size) * num_kv_heads + kvh) * (int64_t)head_dim;"),
+    ("softmax_base_two", "score[t] = exp(score[t] - mx);", "score[t] = exp2(score[t] - mx);"),
+    ("prefill_row_offset_in_batch", "const int i = row - query_start_loc[s];",
+     "const int i = row;"),
+    ("prefill_boundary_row_to_previous_sequence", "while (query_start_loc[s + 1] <= row)",
+     "while (query_start_loc[s + 1] < row)"),
 ]
 
 
