@@ -4,21 +4,25 @@ then decode attention) on synthetic inputs, timed with CUDA events.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 Prints one JSON line (rank 0). ``value`` is microseconds per step (store +
-decode, inputs resident in HBM, L2 flushed between steps); ``roofline``
-reports the decode launch's KV-read bandwidth against the measured HBM copy
-peak; ``e2e`` repeats the step through host buffers (pinned H2D of the step's
-inputs and D2H of its output inside the timed region); ``cpu_baseline`` times
-the fp64 CPU oracle on a bounded sample of the same step and scales it to a
-full step. ``--impl reference`` times only that oracle (the reference arm).
-With N > 1 (torchrun) every rank runs its own replica of the step on its own
-GPU: the path has no cross-GPU exchange.
+decode, inputs resident in HBM, L2 flushed between steps) on the headline
+workload: the skewed long-context decode step (8 sequences of 32k-131k tokens
+among 120 short ones, 32 q / 8 KV heads), the largest of the decode steps.
+``roofline`` reports the decode launch's KV-read bandwidth against the
+measured HBM copy peak; ``e2e`` repeats the step through host buffers (pinned
+H2D of the step's inputs and D2H of its output inside the timed region);
+``cpu_baseline`` times the fp64 CPU oracle on the whole step, on one thread
+and on all host cores. ``workloads`` holds the other decode steps and the two
+prefill steps, each timed the same way (store + call, L2 flushed between
+steps) with its own roofline fraction. ``--impl reference`` times only the
+oracle (the reference arm). With N > 1 (torchrun) every rank runs its own
+replica of the step on its own GPU: the path has no cross-GPU exchange.
 """
 from __future__ import annotations
 
 import argparse
+import dataclasses
 import hashlib
 import json
-import math
 import os
 import re
 import statistics
@@ -36,13 +40,20 @@ sys.path.insert(0, ROOT)
 from paged_kv_cache_255_gb300 import inputs  # noqa: E402
 
 METRIC = "paged-decode µs/step and KV-read GB/s (fraction of GB300 HBM peak)"
-DEFAULT_WORKLOAD = "qwen3_0_6b"
+DEFAULT_WORKLOAD = "long_context"
+# decode and prefill steps measured beside the headline (sub-records)
+SUB_DECODE = ["large_batch", "qwen3_0_6b", "prefix_shared", "tiny"]
+SUB_PREFILL = ["chunked_8b", "qwen3_0_6b_prompts"]
 L2_FLUSH_BYTES = 512 << 20       # > 2x the 129 MB L2
+L2_NOTE = "flushed between steps (512 MiB write)"
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged-prefill µs/step and attention TFLOP/s (fraction of GB300 bf16 tensor peak)"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 KERNEL_SOURCES = ["paged_kv_cache_255_gb300/csrc/decode.cu", "paged_kv_cache_255_gb300/csrc/common.cuh"]
+# a whole oracle step is timed unless one all-cores step would take longer
+# than this; then a sample of the step's outputs is timed and scaled
+FULL_STEP_LIMIT_S = 30.0
 
 
 def kernel_hash() -> str:
@@ -81,9 +92,9 @@ def ncu_traffic(workload: str):
 class ClockSampler:
     """nvidia-smi clock and throttle-reason samples while the GPU is busy."""
 
-    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "clocks_event_reasons.hw_slowdown",
-              "clocks_event_reasons.hw_thermal_slowdown", "clocks_event_reasons.sw_thermal_slowdown",
-              "clocks_event_reasons.sw_power_cap"]
+    FIELDS = ["clocks.sm", "clocks.max.sm", "power.draw", "utilization.gpu",
+              "clocks_event_reasons.hw_slowdown", "clocks_event_reasons.hw_thermal_slowdown",
+              "clocks_event_reasons.sw_thermal_slowdown", "clocks_event_reasons.sw_power_cap"]
 
     def __init__(self, index: int):
         self.proc = None
@@ -130,17 +141,23 @@ class ClockSampler:
             if len(parts) != 1 + len(self.FIELDS):
                 continue
             try:
-                rows.append((float(parts[1]), float(parts[2]), parts[4:]))
+                rows.append((float(parts[1]), float(parts[2]), float(parts[4]), parts[5:]))
             except ValueError:
                 continue
         os.unlink(self.path)
         if not rows:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0,
+                    "samples_under_load": 0}
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for _, _, flags in rows for i, f in enumerate(flags)
+        # samples taken while a kernel was running; the median clock is taken
+        # over those when there are any
+        busy = [r for r in rows if r[2] > 0]
+        use = busy or rows
+        reasons = sorted({names[i] for _, _, _, flags in use for i, f in enumerate(flags)
                           if f.lower() == "active"})
-        return {"sm_mhz": statistics.median(r[0] for r in rows),
-                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows)}
+        return {"sm_mhz": statistics.median(r[0] for r in use),
+                "sm_max_mhz": max(r[1] for r in rows), "reasons": reasons, "samples": len(rows),
+                "samples_under_load": len(busy)}
 
 
 def dist_setup(n_gpus):
@@ -172,61 +189,99 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
-def workload_config(wl):
+def workload_config(wl, q_len=1, layout="token_major"):
     s = wl.spec
     return {"workload": s.name, "num_seqs": wl.num_seqs, "num_q_heads": s.num_q_heads,
             "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
             "num_blocks": wl.num_blocks, "store_rows": int(wl.slot_mapping.shape[0]),
             "context_tokens": int(wl.context_lens.astype(np.int64).sum()),
-            "max_context_len": wl.max_context_len, "seed": wl.seed,
-            "l2": "flushed between steps (512 MiB write)"}
+            "max_context_len": wl.max_context_len, "seed": wl.seed, "l2": L2_NOTE,
+            "q_len": q_len, "layout": layout}
 
 
-def oracle_sample(wl, target_s: float, host=None):
-    """Time the fp64 oracle on a bounded sample of the step and scale to a full
-    step. Returns (us_per_step, threads, sample description)."""
+# ---------------------------------------------------------------------------
+# the fp64 oracle on the host cores (cpu_baseline and the reference arm)
+
+def host_copies(wl):
+    return (wl.q.cpu(), wl.k_cache.cpu(), wl.v_cache.cpu(), wl.k_new.cpu(), wl.v_new.cpu())
+
+
+def oracle_full_step(wl, host, threads: int):
+    """One whole decode step on the oracle: the store of every new row into
+    private copies of the pools (the copies are not timed), then every
+    (sequence, query head) output. Returns (seconds, threads used)."""
     import oracle
     O = oracle.get()
-    threads = O.num_threads()
-    if host is None:
-        host = (wl.q.cpu(), wl.k_cache.cpu(), wl.v_cache.cpu(), wl.k_new.cpu(), wl.v_new.cpu())
     q, kc, vc, kn, vn = host
+    kb, vb = oracle._bits(kc), oracle._bits(vc)
     t_store = 0.0
     if wl.slot_mapping.shape[0]:
-        kc = oracle._bits(kc).copy()            # private pools for the in-place store (untimed)
-        vc = oracle._bits(vc).copy()
+        kb, vb = kb.copy(), vb.copy()
         t0 = time.perf_counter()
-        O.store_kvcache_into(kn, vn, kc, vc, wl.slot_mapping)
+        O.store_kvcache_into(kn, vn, kb, vb, wl.slot_mapping)
+        t_store = time.perf_counter() - t0
+    t0 = time.perf_counter()
+    O.decode(q, kb, vb, wl.block_tables, wl.context_lens, wl.scale, threads=threads)
+    return t_store + time.perf_counter() - t0, (threads if threads > 0 else O.num_threads())
+
+
+def oracle_sampled_step(wl, host, target_s: float, threads: int):
+    """A bounded sample for steps too big to time whole: random (sequence,
+    head) outputs until target_s of oracle time, scaled by context tokens to
+    the whole step; the store is timed whole. Returns (seconds, threads, pairs)."""
+    import oracle
+    O = oracle.get()
+    q, kc, vc, kn, vn = host
+    kb, vb = oracle._bits(kc), oracle._bits(vc)
+    t_store = 0.0
+    if wl.slot_mapping.shape[0]:
+        kb, vb = kb.copy(), vb.copy()
+        t0 = time.perf_counter()
+        O.store_kvcache_into(kn, vn, kb, vb, wl.slot_mapping)
         t_store = time.perf_counter() - t0
     S, Hq = wl.num_seqs, wl.spec.num_q_heads
     work_all = float(wl.context_lens.astype(np.float64).sum()) * Hq
-    rng = np.random.Generator(np.random.PCG64(123))
-    order = rng.permutation(S * Hq)
-    done_pairs, done_work, elapsed, passes = 0, 0.0, 0.0, 0
-    batch = max(threads, 8)
-    # random (sequence, head) outputs, in growing batches, until target_s of
-    # oracle time; a workload smaller than that is repeated whole
-    while elapsed < target_s:
-        pos = done_pairs % (S * Hq)
-        idx = order[pos:pos + batch]
+    order = np.random.Generator(np.random.PCG64(123)).permutation(S * Hq)
+    done, work, elapsed, batch = 0, 0.0, 0.0, 64
+    while elapsed < target_s and done < S * Hq:
+        idx = order[done:done + batch]
         pairs = np.stack([idx // Hq, idx % Hq], 1).astype(np.int32)
         t0 = time.perf_counter()
-        O.decode_pairs(q, kc, vc, wl.block_tables, wl.context_lens, wl.scale, pairs, threads=0)
+        O.decode_pairs(q, kb, vb, wl.block_tables, wl.context_lens, wl.scale, pairs,
+                       threads=threads)
         elapsed += time.perf_counter() - t0
-        done_pairs += len(idx)
-        done_work += float(wl.context_lens[idx // Hq].astype(np.float64).sum())
+        done += len(idx)
+        work += float(wl.context_lens[idx // Hq].astype(np.float64).sum())
         batch = min(batch * 2, 4096)
-    decode_s = elapsed * (work_all / max(done_work, 1.0))
-    us = (t_store + decode_s) * 1e6
-    sample = (f"oracle store of all {int(wl.slot_mapping.shape[0])} rows + decode of "
-              f"{done_pairs} (seq, q-head) outputs drawn at random with repeats (one step "
-              f"has {S * Hq}), {elapsed:.1f} s of oracle time, scaled by context tokens "
-              f"to one full step")
-    return us, threads, sample
+    used = threads if threads > 0 else O.num_threads()
+    return t_store + elapsed * work_all / max(work, 1.0), used, done
 
 
-def workload_spec(args):
-    spec = inputs.SPECS[args.workload]
+def cpu_baseline(wl, host=None):
+    """The oracle timed on the whole step, on one thread and on all host
+    cores (median of three all-cores steps)."""
+    if host is None:
+        host = host_copies(wl)
+    t_all = [oracle_full_step(wl, host, 0) for _ in range(3)]
+    all_s, cores = statistics.median(t for t, _ in t_all), t_all[0][1]
+    S, Hq = wl.num_seqs, wl.spec.num_q_heads
+    what = (f"full step: oracle store of all {int(wl.slot_mapping.shape[0])} new rows + all "
+            f"{S * Hq} (sequence, query head) outputs")
+    if all_s * cores <= FULL_STEP_LIMIT_S:
+        one_s, _ = oracle_full_step(wl, host, 1)
+        one_what = what
+    else:      # one thread would take too long: time a sample of the step
+        one_s, _, n = oracle_sampled_step(wl, host, 15.0, 1)
+        one_what = (f"store of all rows + {n} random (sequence, query head) outputs of "
+                    f"{S * Hq}, scaled by context tokens to the full step")
+    return {"value": all_s * 1e6, "unit": "us/step", "cores": cores, "kind": "oracle",
+            "sample": what,
+            "all_cores": {"value": all_s * 1e6, "cores": cores, "sample": what},
+            "single_thread": {"value": one_s * 1e6, "cores": 1, "sample": one_what}}
+
+
+def workload_spec(args, name=None):
+    spec = inputs.SPECS[name or args.workload]
     if args.num_seqs:
         spec = inputs.scaled(spec, num_seqs=args.num_seqs, name=f"{spec.name}_s{args.num_seqs}")
     return spec
@@ -237,24 +292,171 @@ def run_reference(args, rank, world):
         return
     wl = inputs.generate(workload_spec(args), seed=0,
                          device="cuda" if torch.cuda.is_available() else "cpu")
-    host = (wl.q.cpu(), wl.k_cache.cpu(), wl.v_cache.cpu(), wl.k_new.cpu(), wl.v_new.cpu())
-    # the whole run (warm-up and timed steps) takes about --ref-seconds of oracle time
-    per_step = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
-    for _ in range(args.warmup):
-        oracle_sample(wl, per_step, host)
-    vals = []
+    host = host_copies(wl)
+    # each step is one whole oracle step on all host cores, unless that would
+    # take the run past --ref-seconds; then each step times a sample
+    t_first, threads = oracle_full_step(wl, host, 0)
+    budget = max(0.05, args.ref_seconds / max(1, args.steps + args.warmup))
+    whole = t_first <= max(budget, FULL_STEP_LIMIT_S / max(1, args.steps + args.warmup))
+    S, Hq = wl.num_seqs, wl.spec.num_q_heads
+
+    def one():
+        if whole:
+            t, _ = oracle_full_step(wl, host, 0)
+            return t, (f"full step: oracle store of all {int(wl.slot_mapping.shape[0])} new "
+                       f"rows + all {S * Hq} (sequence, query head) outputs")
+        t, _, n = oracle_sampled_step(wl, host, budget, 0)
+        return t, (f"oracle store of all rows + {n} random (sequence, query head) outputs of "
+                   f"{S * Hq}, scaled by context tokens to the full step")
+
+    for _ in range(max(0, args.warmup - 1)):
+        one()
+    vals, sample = [], ""
     for _ in range(args.steps):
-        us, threads, sample = oracle_sample(wl, per_step, host)
-        vals.append(us)
+        t, sample = one()
+        vals.append(t * 1e6)
     v = statistics.median(vals)
     line = {"impl": "reference", "metric": METRIC, "value": v, "unit": "us/step",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": workload_config(wl),
+            "data": "synthetic", "config": workload_config(wl, args.q_len, args.layout),
             "cpu_baseline": {"value": v, "unit": "us/step", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
+
+
+# ---------------------------------------------------------------------------
+# GPU arm: decode steps
+
+class DecodeStep:
+    """Device buffers and calls of one decode step (store, then decode)."""
+
+    def __init__(self, wl, dev, layout="token_major", q_len=1):
+        from paged_kv_cache_255_gb300 import pagedattn as pa
+        self.pa, self.wl, self.dev = pa, wl, dev
+        s = wl.spec
+        self.HM = layout == "head_major"
+        self.Q = q_len
+        self.k_cache, self.v_cache = wl.k_cache, wl.v_cache
+        if self.HM:          # the same values in a [NB, Hkv, bs, D] pool
+            self.k_cache = self.k_cache.permute(0, 2, 1, 3).contiguous()
+            self.v_cache = self.v_cache.permute(0, 2, 1, 3).contiguous()
+            if q_len > 1:
+                raise SystemExit("--q-len > 1 runs on the token-major layout only")
+        self.q = wl.q
+        if q_len > 1:
+            # q_len query tokens per sequence (speculative verification)
+            gq = torch.Generator(device=dev)
+            gq.manual_seed(1)
+            self.q = torch.randn((wl.num_seqs, q_len, s.num_q_heads, s.head_dim), generator=gq,
+                                 device=dev).to(torch.bfloat16)
+        self.k_new, self.v_new = wl.k_new, wl.v_new
+        self.slots = torch.from_numpy(wl.slot_mapping).to(dev)
+        self.bt = torch.from_numpy(wl.block_tables).to(dev)
+        self.cl = torch.from_numpy(wl.context_lens).to(dev)
+        self.out = torch.empty_like(self.q)
+        self.ws = pa.workspace_for(s.num_q_heads, s.num_kv_heads, s.head_dim, 0, dev)
+        self.has_store = self.slots.shape[0] > 0
+
+    def store(self, kn=None, vn=None, sl=None):
+        if self.has_store:
+            self.pa.store_kvcache(self.k_new if kn is None else kn, self.v_new if vn is None else vn,
+                                  self.k_cache, self.v_cache, self.slots if sl is None else sl,
+                                  head_major=self.HM)
+
+    def decode(self, q=None, bt=None, cl=None):
+        q = self.q if q is None else q
+        bt = self.bt if bt is None else bt
+        cl = self.cl if cl is None else cl
+        if self.Q > 1:
+            return self.pa.decode_multi(q, self.k_cache, self.v_cache, bt, cl, self.wl.scale,
+                                        out=self.out)
+        return self.pa.decode(q, self.k_cache, self.v_cache, bt, cl, self.wl.scale, out=self.out,
+                              workspace=self.ws, head_major=self.HM)
+
+    def step(self):
+        self.store()
+        self.decode()
+
+    def launches_per_step(self):
+        return 3 if self.has_store else 2
+
+
+def time_decode(st: DecodeStep, flush, stream, steps, warmup, world):
+    """Store + decode per step with the L2 flushed before each step: one pass
+    back to back (the step time) and one with an event between the two calls
+    (the split). Returns milliseconds (max over ranks) and the step times."""
+    for _ in range(warmup):
+        flush.zero_()
+        st.step()
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        st.step()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    step_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    ms = max_over_ranks(sum(step_ms) / len(step_ms), world)
+
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        st.store()
+        ev[i][1].record(stream)
+        st.decode()
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    store_ms = [e[0].elapsed_time(e[1]) for e in ev]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in ev]
+    return {"ms": ms, "step_ms": step_ms,
+            "decode_ms": max_over_ranks(sum(dec_ms) / len(dec_ms), world),
+            "store_ms": max_over_ranks(sum(store_ms) / len(store_ms), world)}
+
+
+def decode_rates(st: DecodeStep, t):
+    """Bandwidth figures of a timed decode step."""
+    wl = st.wl
+    s = wl.spec
+    kv_bytes = wl.kv_bytes()
+    peak, peak_src = measured_peaks()
+    dec_s = t["decode_ms"] * 1e-3
+    achieved = kv_bytes / dec_s / 1e9
+    n_valid = int((wl.slot_mapping >= 0).sum())
+    store_bytes = 4 * n_valid * s.num_kv_heads * s.head_dim * 2 + 8 * int(wl.slot_mapping.shape[0])
+    return {
+        "us_per_step": t["ms"] * 1e3, "store_us": t["store_ms"] * 1e3,
+        "decode_us": t["decode_ms"] * 1e3,
+        "median_us_per_step": statistics.median(t["step_ms"]) * 1e3,
+        # store bandwidth: K and V rows read and written, plus the slots read
+        "store_gbs": store_bytes / (t["store_ms"] * 1e-3) / 1e9
+        if st.has_store and t["store_ms"] > 0 else None,
+        "kv_read_gbs": achieved, "hbm_frac": achieved / peak,
+        "unique_kv_read_gbs": wl.unique_kv_bytes() / dec_s / 1e9,
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak,
+                     "traffic": ncu_traffic(s.name) if st.Q == 1 and not st.HM else None,
+                     "kernel": "pa_decode (decode + combine launches)",
+                     "algorithmic_bytes": kv_bytes, "peak_source": f"{peak_src} hbm_gbs"},
+    }
+
+
+def decode_sub_record(name, args, dev, flush, stream, world):
+    wl = inputs.generate(workload_spec(args, name), seed=0, device=dev)
+    st = DecodeStep(wl, dev)
+    t = time_decode(st, flush, stream, args.steps, args.warmup, world)
+    rec = {"config": workload_config(wl), **decode_rates(st, t),
+           "gpu_launches": args.steps * st.launches_per_step()}
+    del st, wl
+    torch.cuda.empty_cache()
+    return rec
 
 
 def run_gpu(args, rank, world, local):
@@ -262,81 +464,18 @@ def run_gpu(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     wl = inputs.generate(workload_spec(args), seed=0, device=dev)
-    S, Hq, Hkv, D = wl.num_seqs, wl.spec.num_q_heads, wl.spec.num_kv_heads, wl.spec.head_dim
-    q = wl.q
-    k_cache, v_cache = wl.k_cache, wl.v_cache
-    HM = args.layout == "head_major"
-    if HM:          # the same values in a [NB, Hkv, bs, D] pool
-        k_cache = k_cache.permute(0, 2, 1, 3).contiguous()
-        v_cache = v_cache.permute(0, 2, 1, 3).contiguous()
-        if args.q_len > 1:
-            raise SystemExit("--q-len > 1 runs on the token-major layout only")
-    k_new, v_new = wl.k_new, wl.v_new
-    slots = torch.from_numpy(wl.slot_mapping).to(dev)
-    bt = torch.from_numpy(wl.block_tables).to(dev)
-    cl = torch.from_numpy(wl.context_lens).to(dev)
-    Q = args.q_len
-    if Q > 1:
-        # Q query tokens per sequence (speculative verification)
-        gq = torch.Generator(device=dev)
-        gq.manual_seed(1)
-        q = torch.randn((S, Q, Hq, D), generator=gq, device=dev).to(torch.bfloat16)
-    out = torch.empty_like(q)
-    ws = pa.workspace_for(Hq, Hkv, D, 0, dev)
-
-    def decode_call(q_, bt_, cl_):
-        if Q > 1:
-            return pa.decode_multi(q_, k_cache, v_cache, bt_, cl_, wl.scale, out=out)
-        return pa.decode(q_, k_cache, v_cache, bt_, cl_, wl.scale, out=out, workspace=ws,
-                         head_major=HM)
+    st = DecodeStep(wl, dev, args.layout, args.q_len)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
-    has_store = slots.shape[0] > 0
 
-    def step():
-        if has_store:
-            pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots, head_major=HM)
-        decode_call(q, bt, cl)
+    # the clock sampler runs from before the first warm-up step to after the
+    # last timed pass (sub-records included)
+    clocks = ClockSampler(local)
+    clocks.wait_first_sample()
 
     # ---- device-resident timing: store then decode back to back, as a user
     # issues them (the decode launch may overlap the store's tail)
-    clocks = ClockSampler(local)
-    clocks.wait_first_sample()
-    for _ in range(args.warmup):
-        flush.zero_()
-        step()
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    step_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    ms = max_over_ranks(sum(step_ms) / len(step_ms), world)
-
-    # ---- the same steps with an event between store and decode, for the
-    # per-call split and the decode launch's own bandwidth (roofline)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        if has_store:
-            pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots, head_major=HM)
-        ev[i][1].record(stream)
-        decode_call(q, bt, cl)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
-    store_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    dec_ms = [ev[i][1].elapsed_time(ev[i][2]) for i in range(args.steps)]
-    dec_avg = max_over_ranks(sum(dec_ms) / len(dec_ms), world)
-    store_avg = max_over_ranks(sum(store_ms) / len(store_ms), world)
+    t = time_decode(st, flush, stream, args.steps, args.warmup, world)
 
     # ---- warm: the same steps without the L2 flush between them (inputs that
     # fit L2 then stay there; informative, not the reported value). A short
@@ -348,37 +487,35 @@ def run_gpu(args, rank, world, local):
     for i in range(args.steps):
         torch.cuda._sleep(100_000)
         ev[i][0].record(stream)
-        step()
+        st.step()
         ev[i][1].record(stream)
     torch.cuda.synchronize()
-    warm_ms = [ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)]
-    warm_avg = max_over_ranks(sum(warm_ms) / len(warm_ms), world)
+    warm_avg = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps, world)
 
     # ---- end to end through host buffers: the step's inputs are packed in one
     # pinned staging buffer, copied in one transfer, and the output read back
-    host_inputs = [q, k_new, v_new, slots, bt, cl]
+    host_inputs = [st.q, st.k_new, st.v_new, st.slots, st.bt, st.cl]
     offs, total = [], 0
-    for t in host_inputs:
+    for x in host_inputs:
         offs.append(total)
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
+        total += (x.numel() * x.element_size() + 255) // 256 * 256
     h_stage = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-    for t, o in zip(host_inputs, offs):
-        n = t.numel() * t.element_size()
-        h_stage[o:o + n].copy_(t.contiguous().view(-1).view(torch.uint8).cpu())
+    for x, o in zip(host_inputs, offs):
+        n = x.numel() * x.element_size()
+        h_stage[o:o + n].copy_(x.contiguous().view(-1).view(torch.uint8).cpu())
     d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
-    views = [d_stage[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-             for t, o in zip(host_inputs, offs)]
+    views = [d_stage[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape)
+             for x, o in zip(host_inputs, offs)]
     dq, dk, dv, ds, dbt, dcl = views
-    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
+    hout = torch.empty(st.out.shape, dtype=st.out.dtype, pin_memory=True)
+    h2d = sum(x.numel() * x.element_size() for x in host_inputs)
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
         d_stage.copy_(h_stage, non_blocking=True)
-        if has_store:
-            pa.store_kvcache(dk, dv, k_cache, v_cache, ds, head_major=HM)
-        decode_call(dq, dbt, dcl)
-        hout.copy_(out, non_blocking=True)
+        st.store(dk, dv, ds)
+        st.decode(dq, dbt, dcl)
+        hout.copy_(st.out, non_blocking=True)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -395,7 +532,7 @@ def run_gpu(args, rank, world, local):
         e2e_ms.append(a_.elapsed_time(b_))
     e2e = max_over_ranks(sum(e2e_ms) / len(e2e_ms), world)
     torch.cuda.synchronize()
-    if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
+    if not torch.equal(hout.view(torch.int16), st.out.cpu().view(torch.int16)):
         raise SystemExit("e2e output differs from the device-resident output")
 
     # ---- the same two steps replayed from CUDA graphs (one launch per step)
@@ -404,7 +541,7 @@ def run_gpu(args, rank, world, local):
             flush.zero_()
             g.replay()
         torch.cuda.synchronize()
-        t = []
+        ts = []
         for _ in range(args.steps):
             flush.zero_()
             a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -412,68 +549,76 @@ def run_gpu(args, rank, world, local):
             g.replay()
             b_.record(stream)
             b_.synchronize()
-            t.append(a_.elapsed_time(b_))
-        return max_over_ranks(sum(t) / len(t), world)
-
-    def time_graphs():
-        g_dev = pa.DecodeStepGraph(q, k_cache, v_cache, bt, cl, wl.scale, k_new=k_new, v_new=v_new,
-                                   slot_mapping=slots if has_store else None, out=out,
-                                   head_major=HM)
-        graph_ms = time_replay(g_dev)
-        g_e2e = pa.DecodeStepGraph(dq, k_cache, v_cache, dbt, dcl, wl.scale, k_new=dk, v_new=dv,
-                                   slot_mapping=ds if has_store else None, out=out,
-                                   host_stage=h_stage, device_stage=d_stage, host_out=hout,
-                                   head_major=HM)
-        graph_e2e_ms = time_replay(g_e2e)
-        torch.cuda.synchronize()
-        if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
-            raise SystemExit("graph e2e output differs from the device-resident output")
-        return graph_ms, graph_e2e_ms
+            ts.append(a_.elapsed_time(b_))
+        return max_over_ranks(sum(ts) / len(ts), world)
 
     graph_ms = graph_e2e_ms = float("nan")
-    if Q == 1:
-        graph_ms, graph_e2e_ms = time_graphs()
+    if st.Q == 1:
+        sl = st.slots if st.has_store else None
+        g_dev = pa.DecodeStepGraph(st.q, st.k_cache, st.v_cache, st.bt, st.cl, wl.scale,
+                                   k_new=st.k_new, v_new=st.v_new, slot_mapping=sl, out=st.out,
+                                   head_major=st.HM)
+        graph_ms = time_replay(g_dev)
+        g_e2e = pa.DecodeStepGraph(dq, st.k_cache, st.v_cache, dbt, dcl, wl.scale, k_new=dk,
+                                   v_new=dv, slot_mapping=ds if st.has_store else None,
+                                   out=st.out, host_stage=h_stage, device_stage=d_stage,
+                                   host_out=hout, head_major=st.HM)
+        graph_e2e_ms = time_replay(g_e2e)
+        torch.cuda.synchronize()
+        if not torch.equal(hout.view(torch.int16), st.out.cpu().view(torch.int16)):
+            raise SystemExit("graph e2e output differs from the device-resident output")
+        del g_dev, g_e2e
+
+    host = host_copies(wl) if rank == 0 and not args.no_cpu_baseline else None
+    # the step's structure (lengths, tables, slots) for the CPU baseline; its
+    # values are in the host copies, and the device pools are freed below
+    wl_struct = dataclasses.replace(wl, q=None, k_new=None, v_new=None, k_cache=None,
+                                    v_cache=None)
+    rates = decode_rates(st, t)
+    config = workload_config(wl, st.Q, args.layout)
+    launches = args.steps * st.launches_per_step()
+    del st, wl, views, dq, dk, dv, ds, dbt, dcl, d_stage
+    torch.cuda.empty_cache()
+
+    # ---- the other decode steps and the prefill steps, timed the same way
+    subs = {}
+    if not args.no_sub_records:
+        for name in SUB_DECODE:
+            if name != args.workload:
+                subs[name] = decode_sub_record(name, args, dev, flush, stream, world)
+        for name in SUB_PREFILL:
+            subs[name] = prefill_sub_record(name, args, dev, flush, stream, world)
+    clk = clocks.stop()
 
     if rank != 0:
         return
-    kv_bytes = wl.kv_bytes()
-    peak, peak_src = measured_peaks()
-    achieved = kv_bytes / (dec_avg * 1e-3) / 1e9
     line = {
-        "metric": METRIC, "value": ms * 1e3, "unit": "us/step", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms,
+        "metric": METRIC, "value": rates["us_per_step"], "unit": "us/step", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": t["ms"],
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": dict(workload_config(wl), q_len=Q, layout=args.layout),
-        "store_us": store_avg * 1e3, "decode_us": dec_avg * 1e3,
-        "median_us_per_step": statistics.median(step_ms) * 1e3,
+        "data": "synthetic", "config": config,
+        **{k: v for k, v in rates.items() if k != "us_per_step"},
         "warm_us_per_step": warm_avg * 1e3,
-        # store bandwidth: K and V rows read and written, plus the slots read
-        "store_gbs": (4 * int((wl.slot_mapping >= 0).sum()) * Hkv * D * 2 + 8 * int(wl.slot_mapping.shape[0]))
-                     / (store_avg * 1e-3) / 1e9 if has_store and store_avg > 0 else None,
-        "kv_read_gbs": achieved, "hbm_frac": achieved / peak,
-        "unique_kv_read_gbs": wl.unique_kv_bytes() / (dec_avg * 1e-3) / 1e9,
-        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak,
-                     "traffic": ncu_traffic(wl.spec.name) if Q == 1 and not HM else None,
-                     "kernel": "pa_decode (decode + combine launches)",
-                     "algorithmic_bytes": kv_bytes, "peak_source": f"{peak_src} hbm_gbs"},
         "e2e": {"value": e2e * 1e3, "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
-        "graph": {"us_per_step": graph_ms * 1e3 if Q == 1 else None,
-                  "e2e_us_per_step": graph_e2e_ms * 1e3 if Q == 1 else None,
+        "graph": {"us_per_step": graph_ms * 1e3 if args.q_len == 1 else None,
+                  "e2e_us_per_step": graph_e2e_ms * 1e3 if args.q_len == 1 else None,
                   "note": "store + decode (and, for e2e, the H2D and D2H copies) captured "
                           "in one CUDA graph, one replay per step"},
-        "gpu_launches": args.steps * (3 if has_store else 2),
+        "gpu_launches": launches,
         "timing": "value: store + decode back to back per step; store_us / decode_us: a "
-                  "second pass with an event between the two calls",
+                  "second pass with an event between the two calls; workloads: the same "
+                  "two passes on each other step",
         "clocks": clk,
+        "workloads": subs,
     }
-    if not args.no_cpu_baseline and world >= 1:
-        us, threads, sample = oracle_sample(wl, args.cpu_seconds)
-        line["cpu_baseline"] = {"value": us, "unit": "us/step", "cores": threads,
-                                "kind": "oracle", "sample": sample}
+    if host is not None:
+        line["cpu_baseline"] = cpu_baseline(wl_struct, host)
     print(json.dumps(line), flush=True)
 
+
+# ---------------------------------------------------------------------------
+# GPU arm: prefill steps
 
 def prefill_flops(pb) -> int:
     """Algorithmic FLOPs of one prefill launch: per causal (row, key) pair and
@@ -482,8 +627,9 @@ def prefill_flops(pb) -> int:
     return 4 * pb.wl.spec.head_dim * pb.wl.spec.num_q_heads * pb.causal_pairs()
 
 
-def prefill_config(pb, chunk):
-    c = workload_config(pb.wl)
+def prefill_config(pb, chunk, layout="token_major"):
+    c = workload_config(pb.wl, 1, layout)
+    c.pop("q_len")
     c.update(store_rows=int(pb.slot_mapping.shape[0]), query_rows=int(pb.query_start_loc[-1]),
              max_query_len=pb.max_query_len, chunk="whole prompt" if chunk is None else chunk,
              causal_pairs=pb.causal_pairs())
@@ -529,8 +675,8 @@ def prefill_oracle_sample(pb, target_s: float, host=None):
     return us, threads, sample
 
 
-def prefill_spec(args):
-    spec, chunk = inputs.PREFILL_SPECS[args.workload]
+def prefill_spec(args, name=None):
+    spec, chunk = inputs.PREFILL_SPECS[name or args.workload]
     if args.num_seqs:
         spec = inputs.scaled(spec, num_seqs=args.num_seqs, name=f"{spec.name}_s{args.num_seqs}")
     return spec, chunk
@@ -552,85 +698,129 @@ def run_reference_prefill(args, rank, world):
     line = {"impl": "reference", "metric": PREFILL_METRIC, "value": v, "unit": "us/step",
             "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": v / 1e3,
             "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-            "data": "synthetic", "config": prefill_config(pb, chunk),
+            "data": "synthetic", "config": prefill_config(pb, chunk, args.layout),
             "cpu_baseline": {"value": v, "unit": "us/step", "cores": threads, "kind": "oracle",
                              "sample": sample},
             "e2e": {"value": v, "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
 
+class PrefillStep:
+    """Device buffers and calls of one prefill step (store of the chunk rows,
+    then paged prefill)."""
+
+    def __init__(self, pb, dev, layout="token_major"):
+        from paged_kv_cache_255_gb300 import pagedattn as pa
+        self.pa, self.pb = pa, pb
+        wl = pb.wl
+        self.k_cache, self.v_cache = wl.k_cache.to(dev), wl.v_cache.to(dev)
+        self.HM = layout == "head_major"
+        if self.HM:          # the same values in a [NB, Hkv, bs, D] pool
+            self.k_cache = self.k_cache.permute(0, 2, 1, 3).contiguous()
+            self.v_cache = self.v_cache.permute(0, 2, 1, 3).contiguous()
+        self.host_inputs = [pb.q, pb.k_new, pb.v_new, torch.from_numpy(pb.slot_mapping),
+                            torch.from_numpy(wl.block_tables), torch.from_numpy(wl.context_lens),
+                            torch.from_numpy(pb.query_start_loc)]
+        self.args = [t.to(dev) for t in self.host_inputs]
+        self.out = torch.empty_like(self.args[0])
+        self.mql = pb.max_query_len
+
+    def store(self, kn, vn, sl):
+        self.pa.store_kvcache(kn, vn, self.k_cache, self.v_cache, sl, head_major=self.HM)
+
+    def prefill(self, q, bt, cl, qsl):
+        self.pa.prefill(q, self.k_cache, self.v_cache, bt, cl, qsl, self.pb.wl.scale,
+                        max_query_len=self.mql, out=self.out, head_major=self.HM)
+
+    def step(self, q, kn, vn, sl, bt, cl, qsl):
+        self.store(kn, vn, sl)
+        self.prefill(q, bt, cl, qsl)
+
+
+def time_prefill(ps: PrefillStep, flush, stream, steps, warmup, world):
+    q, kn, vn, sl, bt, cl, qsl = ps.args
+    for _ in range(warmup):
+        flush.zero_()
+        ps.step(*ps.args)
+    torch.cuda.synchronize()
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
+    barrier(world)
+    torch.cuda.synchronize()
+    for i in range(steps):
+        flush.zero_()
+        ev[i][0].record(stream)
+        ps.store(kn, vn, sl)
+        ev[i][1].record(stream)
+        ps.prefill(q, bt, cl, qsl)
+        ev[i][2].record(stream)
+    torch.cuda.synchronize()
+    barrier(world)
+    return {"ms": max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in ev), world),
+            "store_ms": max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev), world),
+            "prefill_ms": max_over_ranks(statistics.mean(e[1].elapsed_time(e[2]) for e in ev), world)}
+
+
+def prefill_rates(pb, t):
+    flops = prefill_flops(pb)
+    peak, peak_src = measured_peaks("bf16_tflops")
+    achieved = flops / (t["prefill_ms"] * 1e-3) / 1e12
+    return {"us_per_step": t["ms"] * 1e3, "store_us": t["store_ms"] * 1e3,
+            "prefill_us": t["prefill_ms"] * 1e3,
+            "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
+                         "frac": achieved / peak, "traffic": None, "kernel": "pa_prefill",
+                         "algorithmic_flops": flops,
+                         "peak_source": f"{peak_src} bf16_tflops (burst)"}}
+
+
+def prefill_sub_record(name, args, dev, flush, stream, world):
+    spec, chunk = prefill_spec(args, name)
+    pb = inputs.prefill_batch(spec, seed=0, chunk=chunk)
+    ps = PrefillStep(pb, dev)
+    steps = max(3, min(args.steps, 10))
+    t = time_prefill(ps, flush, stream, steps, args.warmup, world)
+    rec = {"metric": PREFILL_METRIC, "config": prefill_config(pb, chunk), "steps": steps,
+           **prefill_rates(pb, t), "gpu_launches": steps * 2}
+    del ps, pb
+    torch.cuda.empty_cache()
+    return rec
+
+
 def run_gpu_prefill(args, rank, world, local):
     """One prefill step: store of every chunk row's K/V, then paged prefill."""
-    from paged_kv_cache_255_gb300 import pagedattn as pa
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     spec, chunk = prefill_spec(args)
     pb = inputs.prefill_batch(spec, seed=0, chunk=chunk)
-    wl = pb.wl
-    k_cache, v_cache = wl.k_cache.to(dev), wl.v_cache.to(dev)
-    HM = args.layout == "head_major"
-    if HM:          # the same values in a [NB, Hkv, bs, D] pool
-        k_cache = k_cache.permute(0, 2, 1, 3).contiguous()
-        v_cache = v_cache.permute(0, 2, 1, 3).contiguous()
-    host_inputs = [pb.q, pb.k_new, pb.v_new, torch.from_numpy(pb.slot_mapping),
-                   torch.from_numpy(wl.block_tables), torch.from_numpy(wl.context_lens),
-                   torch.from_numpy(pb.query_start_loc)]
-    q, k_new, v_new, slots, bt, cl, qsl = [t.to(dev) for t in host_inputs]
-    out = torch.empty_like(q)
-    mql = pb.max_query_len
+    ps = PrefillStep(pb, dev, args.layout)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
 
-    def step(q_, kn_, vn_, sl_, bt_, cl_, qsl_):
-        pa.store_kvcache(kn_, vn_, k_cache, v_cache, sl_, head_major=HM)
-        pa.prefill(q_, k_cache, v_cache, bt_, cl_, qsl_, wl.scale, max_query_len=mql, out=out,
-                   head_major=HM)
-
     clocks = ClockSampler(local)
     clocks.wait_first_sample()
-    for _ in range(args.warmup):
-        flush.zero_()
-        step(q, k_new, v_new, slots, bt, cl, qsl)
-    torch.cuda.synchronize()
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
-    barrier(world)
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        flush.zero_()
-        ev[i][0].record(stream)
-        pa.store_kvcache(k_new, v_new, k_cache, v_cache, slots, head_major=HM)
-        ev[i][1].record(stream)
-        pa.prefill(q, k_cache, v_cache, bt, cl, qsl, wl.scale, max_query_len=mql, out=out,
-                   head_major=HM)
-        ev[i][2].record(stream)
-    torch.cuda.synchronize()
-    barrier(world)
-    clk = clocks.stop()
-    step_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[2]) for e in ev), world)
-    store_ms = max_over_ranks(statistics.mean(e[0].elapsed_time(e[1]) for e in ev), world)
-    pf_ms = max_over_ranks(statistics.mean(e[1].elapsed_time(e[2]) for e in ev), world)
+    t = time_prefill(ps, flush, stream, args.steps, args.warmup, world)
 
     # end to end: pinned host inputs packed in one staging buffer, one H2D,
     # the step, the output read back
+    host_inputs = ps.host_inputs
     offs, total = [], 0
-    for t in host_inputs:
+    for x in host_inputs:
         offs.append(total)
-        total += (t.numel() * t.element_size() + 255) // 256 * 256
+        total += (x.numel() * x.element_size() + 255) // 256 * 256
     h_stage = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-    for t, o in zip(host_inputs, offs):
-        nb = t.numel() * t.element_size()
-        h_stage[o:o + nb].copy_(t.contiguous().view(-1).view(torch.uint8))
+    for x, o in zip(host_inputs, offs):
+        nb = x.numel() * x.element_size()
+        h_stage[o:o + nb].copy_(x.contiguous().view(-1).view(torch.uint8))
     d_stage = torch.empty(total, dtype=torch.uint8, device=dev)
-    views = [d_stage[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
-             for t, o in zip(host_inputs, offs)]
-    hout = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(t.numel() * t.element_size() for t in host_inputs)
+    views = [d_stage[o:o + x.numel() * x.element_size()].view(x.dtype).view(x.shape)
+             for x, o in zip(host_inputs, offs)]
+    hout = torch.empty(ps.out.shape, dtype=ps.out.dtype, pin_memory=True)
+    h2d = sum(x.numel() * x.element_size() for x in host_inputs)
     d2h = hout.numel() * hout.element_size()
 
     def e2e_step():
         d_stage.copy_(h_stage, non_blocking=True)
-        step(*views)
-        hout.copy_(out, non_blocking=True)
+        ps.step(*views)
+        hout.copy_(ps.out, non_blocking=True)
 
     for _ in range(args.warmup):
         flush.zero_()
@@ -647,23 +837,18 @@ def run_gpu_prefill(args, rank, world, local):
         e2e_ms.append(a_.elapsed_time(b_))
     e2e = max_over_ranks(statistics.mean(e2e_ms), world)
     torch.cuda.synchronize()
-    if not torch.equal(hout.view(torch.int16), out.cpu().view(torch.int16)):
+    clk = clocks.stop()
+    if not torch.equal(hout.view(torch.int16), ps.out.cpu().view(torch.int16)):
         raise SystemExit("e2e output differs from the device-resident output")
     if rank != 0:
         return
-    flops = prefill_flops(pb)
-    peak, peak_src = measured_peaks("bf16_tflops")
-    achieved = flops / (pf_ms * 1e-3) / 1e12
+    rates = prefill_rates(pb, t)
     line = {
-        "metric": PREFILL_METRIC, "value": step_ms * 1e3, "unit": "us/step", "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": step_ms,
+        "metric": PREFILL_METRIC, "value": rates["us_per_step"], "unit": "us/step",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": t["ms"],
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
-        "data": "synthetic", "config": dict(prefill_config(pb, chunk), layout=args.layout),
-        "store_us": store_ms * 1e3, "prefill_us": pf_ms * 1e3,
-        "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                     "frac": achieved / peak, "traffic": None, "kernel": "pa_prefill",
-                     "algorithmic_flops": flops,
-                     "peak_source": f"{peak_src} bf16_tflops (burst)"},
+        "data": "synthetic", "config": prefill_config(pb, chunk, args.layout),
+        **{k: v for k, v in rates.items() if k != "us_per_step"},
         "e2e": {"value": e2e * 1e3, "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "gpu_launches": args.steps * 2,
@@ -692,9 +877,12 @@ def main():
     ap.add_argument("--layout", default="token_major", choices=["token_major", "head_major"],
                     help="KV pool layout: [NB, bs, Hkv, D] or [NB, Hkv, bs, D]")
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
-    ap.add_argument("--cpu-seconds", type=float, default=15.0)
+    ap.add_argument("--cpu-seconds", type=float, default=15.0,
+                    help="oracle time of the prefill CPU baseline's sample")
     ap.add_argument("--ref-seconds", type=float, default=60.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-sub-records", action="store_true",
+                    help="time the chosen workload only (profiling runs)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
