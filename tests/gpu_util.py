@@ -12,6 +12,21 @@ ATOL = 2e-2
 RTOL = 2e-2
 
 
+def decode_kernel(name: str):
+    """Run the following decode calls on the tensor-core tiles ("mma", the
+    product kernel) or the CUDA-core tiles ("simt", kept for tests); the
+    conftest resets the choice after every test."""
+    assert name in ("mma", "simt"), name
+    pa.debug_kernel_variant(pa.VARIANT_DECODE_SIMT if name == "simt" else 0)
+
+
+def prefill_kernel(name: str):
+    """Run the following prefill calls on the tcgen05 kernel ("tc", the
+    product kernel) or the mma.sync kernel ("mma", kept for tests)."""
+    assert name in ("tc", "mma"), name
+    pa.debug_kernel_variant(pa.VARIANT_PREFILL_MMA if name == "mma" else 0)
+
+
 def device_inputs(wl, dev="cuda"):
     """Device copies of a workload (caches cloned: the store writes them)."""
     d = dict(
@@ -43,16 +58,48 @@ def host_bits(t: torch.Tensor) -> np.ndarray:
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view(np.uint16)
 
 
-def assert_close(gpu_out: torch.Tensor, ref: np.ndarray, what: str = ""):
-    got = gpu_out.detach().float().cpu().double().numpy()
+# Per (sequence, head) output row, the relative L2 error ||gpu - ref|| / ||ref||
+# must stay below ROW_REL_L2. The element-wise bound above is the stated
+# contract, but at long context every |ref| is ~0.02 or less (a convex
+# combination of ~L independent N(0,1) rows has sigma ~ sqrt(e / L)), so the
+# bound is about 0.02 absolute and an all-zero row would pass it. Rounding
+# P to bf16 (the tensor-core P.V operand) and the output to bf16 give a
+# relative row error of about 2.5e-3 at any length (simulated for L = 2 ..
+# 65536), so 1e-2 leaves a 4x margin while a zero row scores 1 and another
+# head's row about 1.4.
+ROW_REL_L2 = 1e-2
+ROW_ABS_FLOOR = 1e-6      # rows whose reference is exactly zero (no visible token)
+
+
+def close_report(got: np.ndarray, ref: np.ndarray):
+    """None if ``got`` matches ``ref`` (both float64, rows along the last
+    axis) under both bounds, else a message naming the first failure."""
     assert got.shape == ref.shape, (got.shape, ref.shape)
-    assert np.isfinite(got).all(), f"{what}: non-finite output"
+    if not np.isfinite(got).all():
+        return "non-finite output"
     err = np.abs(got - ref)
-    bound = ATOL + RTOL * np.abs(ref)
-    bad = err > bound
+    bad = err > ATOL + RTOL * np.abs(ref)
     if bad.any():
-        idx = np.argwhere(bad)[0]
-        raise AssertionError(f"{what}: {int(bad.sum())} elements out of tolerance; first at "
-                             f"{tuple(idx)}: gpu {got[tuple(idx)]} ref {ref[tuple(idx)]}; "
-                             f"max err {err.max()}")
-    return float(err.max())
+        idx = tuple(np.argwhere(bad)[0])
+        return (f"{int(bad.sum())} elements out of tolerance; first at {idx}: gpu {got[idx]} "
+                f"ref {ref[idx]}; max err {err.max()}")
+    d = got.shape[-1]
+    num = np.linalg.norm((got - ref).reshape(-1, d), axis=1)
+    den = np.linalg.norm(ref.reshape(-1, d), axis=1)
+    row_bad = num > ROW_REL_L2 * den + ROW_ABS_FLOOR
+    if row_bad.any():
+        r = int(np.argmax(row_bad))
+        return (f"{int(row_bad.sum())} rows above relative L2 error {ROW_REL_L2}; first is row "
+                f"{np.unravel_index(r, got.shape[:-1])}: |gpu - ref| {num[r]:.3g}, |ref| {den[r]:.3g}")
+    return None
+
+
+def assert_close(gpu_out, ref: np.ndarray, what: str = ""):
+    if isinstance(gpu_out, torch.Tensor):
+        got = gpu_out.detach().float().cpu().double().numpy()
+    else:
+        got = np.asarray(gpu_out, dtype=np.float64)
+    msg = close_report(got, ref)
+    if msg is not None:
+        raise AssertionError(f"{what}: {msg}")
+    return float(np.abs(got - ref).max()) if got.size else 0.0
