@@ -179,7 +179,10 @@ PA_API pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const vo
  *
  * - The first call on a device looks up the array's device address (with
  *   that device current) and caches it; make that first call before any
- *   stream capture.
+ *   stream capture. The cached address belongs to the CUDA context that was
+ *   current then: after cudaDeviceReset (or any reset of the device's
+ *   primary context) the library's module is loaded again at a new address,
+ *   so this call is not supported after such a reset in the same process.
  * - Every call shares the one array. Nothing in it needs to start at zero
  *   (each call writes every word it later reads), but calls that overlap on
  *   the GPU (on different streams, or from different threads) race on it
@@ -188,7 +191,10 @@ PA_API pa_status_t pa_decode_splitk(const void *q, const void *k_cache, const vo
  *   (pa_decode_workspace_size(...) > PA_NOALLOC_SCRATCH_BYTES; on a 152-SM
  *   GB300 that is a group size above 8) returns PA_ERR_WORKSPACE and
  *   launches nothing.
- * Results equal pa_decode's for the same inputs.
+ * Argument checks and their statuses are pa_decode's (an empty batch
+ * returns PA_OK without touching a device); a failed device query returns
+ * PA_ERR_CUDA. Results are bit-identical to pa_decode's for the same inputs
+ * on the same device.
  */
 #define PA_NOALLOC_SCRATCH_BYTES (16u << 20)
 PA_API pa_status_t pa_decode_noalloc(const void *q, const void *k_cache, const void *v_cache,
@@ -326,6 +332,23 @@ PA_API pa_status_t pa_take_device_error(int32_t *code, void *stream);
  * restores normal launches. Process-wide; for tests only.
  */
 PA_API pa_status_t pa_debug_prefill_fault(int mode);
+
+/*
+ * Test hook, off by default: run the comparison kernels the library keeps
+ * for testing instead of the product kernels. flags is 0 (the product
+ * kernels) or an OR of
+ *   PA_VARIANT_DECODE_SIMT  decode tiles on the CUDA cores instead of the
+ *                           tensor cores (single-token decode, group size
+ *                           <= 8; other calls keep the tensor cores);
+ *   PA_VARIANT_PREFILL_MMA  pa_prefill on the mma.sync kernel instead of the
+ *                           tcgen05 kernel.
+ * Both compute the same results within the tolerance of the product kernels;
+ * the tests use them as a second parity path. Process-wide, read at each
+ * call; PA_ERR_INVALID_ARG for an unknown bit. Not for production use.
+ */
+#define PA_VARIANT_DECODE_SIMT 1
+#define PA_VARIANT_PREFILL_MMA 2
+PA_API pa_status_t pa_debug_kernel_variant(int flags);
 
 #ifdef __cplusplus
 }

@@ -1,9 +1,8 @@
 // C ABI of libpagedattn: argument checks on the host, then kernel launches.
 // The public contract is in include/pagedattn.h.
+#include <atomic>
 #include <cmath>
 #include <cstdint>
-#include <cstdlib>
-#include <cstring>
 
 #include <nvtx3/nvToolsExt.h>
 
@@ -53,12 +52,16 @@ int current_sm_count() {
     return n;
 }
 
-// Tile computation for decode: tensor cores unless PA_DECODE_KERNEL=simt asks
-// for the CUDA-core variant (kept for comparison and testing). Group sizes
-// above 8 always use the tensor cores.
+// Comparison kernels kept for tests (pa_debug_kernel_variant); 0 = the
+// product kernels. Read once per call, so a test that flips it between
+// calls sees the change at the next call.
+std::atomic<int> g_kernel_variant{0};
+
+// Tile computation for decode: tensor cores, unless the test hook asks for
+// the CUDA-core variant (single-token decode, group size <= 8).
 pa::DecodeKernel decode_kernel_choice(int group_pad, int q_len) {
-    const char *e = std::getenv("PA_DECODE_KERNEL");
-    if (e && std::strcmp(e, "simt") == 0 && group_pad <= 8 && q_len == 1)
+    if ((g_kernel_variant.load(std::memory_order_relaxed) & PA_VARIANT_DECODE_SIMT) &&
+        group_pad <= 8 && q_len == 1)
         return pa::DecodeKernel::kSimt;
     return pa::DecodeKernel::kMma;
 }
@@ -76,22 +79,14 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                         int block_size, int64_t num_blocks, int layout, void *workspace,
                         size_t workspace_bytes, int num_partitions, void *stream) {
-    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 ||
-        max_blocks_per_seq < 0 || num_partitions < 0 || q_len < 1 || !std::isfinite(scale))
-        return PA_ERR_INVALID_ARG;
-    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
-    if (layout != PA_LAYOUT_TOKEN_MAJOR && layout != PA_LAYOUT_HEAD_MAJOR) return PA_ERR_INVALID_ARG;
-    if (head_dim != pa::kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+    bool nothing_to_do = false;
+    const pa_status_t chk = pa::decode_check_args(
+        q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, q_len, scale, out,
+        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, layout,
+        num_partitions, &nothing_to_do);
+    if (chk != PA_OK || nothing_to_do) return chk;
     const int group = num_q_heads / num_kv_heads;
-    if (q_len > 16) return PA_ERR_UNSUPPORTED;
     const int gp = pa::decode_group_pad(group * q_len);
-    if (gp == 0) return PA_ERR_UNSUPPORTED;
-    if (num_seqs == 0) return PA_OK;
-    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
-        return PA_ERR_INVALID_ARG;
-    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
-        return PA_ERR_INVALID_ARG;
-    if (max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_INVALID_ARG;
 
     const pa::DecodeKernel kind = decode_kernel_choice(gp, q_len);
     const int P = plan_workers(gp, kind, num_partitions);
@@ -187,13 +182,45 @@ pa_status_t prefill_impl(const void *q, const void *k_cache, const void *v_cache
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);
     const int mql = max_query_len > 0 ? max_query_len : 1;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    const char *k = std::getenv("PA_PREFILL_KERNEL");
-    const cudaError_t e = (k && std::strcmp(k, "mma") == 0) ? pa::launch_prefill(a, gp, mql, st)
-                                                            : pa::launch_prefill_tc(a, gp, mql, st);
+    const bool mma = g_kernel_variant.load(std::memory_order_relaxed) & PA_VARIANT_PREFILL_MMA;
+    const cudaError_t e = mma ? pa::launch_prefill(a, gp, mql, st)
+                              : pa::launch_prefill_tc(a, gp, mql, st);
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
 }
 
 }  // namespace
+
+namespace pa {
+
+pa_status_t decode_check_args(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int q_len, float scale,
+                              const void *out, int num_seqs, int num_q_heads, int num_kv_heads,
+                              int head_dim, int block_size, int64_t num_blocks, int layout,
+                              int num_partitions, bool *nothing_to_do) {
+    *nothing_to_do = false;
+    if (num_seqs < 0 || num_q_heads <= 0 || num_kv_heads <= 0 || num_blocks < 0 ||
+        max_blocks_per_seq < 0 || num_partitions < 0 || q_len < 1 || !std::isfinite(scale))
+        return PA_ERR_INVALID_ARG;
+    if (num_q_heads % num_kv_heads != 0) return PA_ERR_INVALID_ARG;
+    if (layout != PA_LAYOUT_TOKEN_MAJOR && layout != PA_LAYOUT_HEAD_MAJOR) return PA_ERR_INVALID_ARG;
+    if (head_dim != kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+    const int group = num_q_heads / num_kv_heads;
+    if (q_len > 16) return PA_ERR_UNSUPPORTED;
+    if (decode_group_pad(group * q_len) == 0) return PA_ERR_UNSUPPORTED;
+    if (num_seqs == 0) {
+        *nothing_to_do = true;
+        return PA_OK;
+    }
+    if (!q || !k_cache || !v_cache || !block_tables || !context_lens || !out)
+        return PA_ERR_INVALID_ARG;
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return PA_ERR_INVALID_ARG;
+    if (max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
+
+}  // namespace pa
 
 extern "C" {
 
@@ -342,6 +369,12 @@ pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const void *v_
                         query_start_loc, max_query_len, scale, out, num_seqs, total_q,
                         num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, layout,
                         stream);
+}
+
+pa_status_t pa_debug_kernel_variant(int flags) {
+    if (flags & ~(PA_VARIANT_DECODE_SIMT | PA_VARIANT_PREFILL_MMA)) return PA_ERR_INVALID_ARG;
+    g_kernel_variant.store(flags, std::memory_order_relaxed);
+    return PA_OK;
 }
 
 pa_status_t pa_debug_prefill_fault(int mode) {

@@ -5,6 +5,8 @@
 #include <cstdint>
 #include <cuda_runtime.h>
 
+#include "../../include/pagedattn.h"
+
 namespace pa {
 
 constexpr int kHeadDimPublic = 128;   // head_dim the ABI accepts
@@ -38,6 +40,16 @@ struct DecodeArgs {
     int num_workers;            // P: contiguous shares of the tile space
     int min_tiles;              // fewest tiles a share may hold (1 = exactly P shares)
 };
+
+// Host-side argument checks of every decode entry point, in the order the
+// calls apply them (pointers, sizes, layout, head_dim, block size, group
+// size; no CUDA call). PA_OK with *nothing_to_do set for an empty batch.
+pa_status_t decode_check_args(const void *q, const void *k_cache, const void *v_cache,
+                              const int32_t *block_tables, int max_blocks_per_seq,
+                              const int32_t *context_lens, int q_len, float scale,
+                              const void *out, int num_seqs, int num_q_heads, int num_kv_heads,
+                              int head_dim, int block_size, int64_t num_blocks, int layout,
+                              int num_partitions, bool *nothing_to_do);
 
 // Padded group size the kernels are instantiated for (power of two >= group,
 // at most 16), or 0 when unsupported.

@@ -24,7 +24,9 @@ void *g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the scratch array on the current device. In host code the
 // array's name is only a host-side stand-in, so the address is looked up once
-// per device with that device current, and cached.
+// per device with that device current, and cached. The cache assumes the
+// device's context is never reset in this process (a reset reloads the module
+// at another address); the header states that limit.
 pa_status_t scratch_on_current_device(void **out) {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return PA_ERR_CUDA;
@@ -46,8 +48,17 @@ extern "C" pa_status_t pa_decode_noalloc(const void *q, const void *k_cache, con
                                          int num_seqs, int num_q_heads, int num_kv_heads,
                                          int head_dim, int block_size, int64_t num_blocks,
                                          void *stream) {
+    // pa_decode's own argument checks first, so that both calls answer bad
+    // arguments and empty batches with the same status
+    bool nothing_to_do = false;
+    const pa_status_t chk = pa::decode_check_args(
+        q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1, scale, out,
+        num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+        PA_LAYOUT_TOKEN_MAJOR, 0, &nothing_to_do);
+    if (chk != PA_OK || nothing_to_do) return chk;
+    // the configuration is valid, so a zero size means the device query failed
     const size_t need = pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim, 0);
-    if (need == 0) return PA_ERR_UNSUPPORTED;
+    if (need == 0) return PA_ERR_CUDA;
     if (need > kNoAllocScratchBytes) return PA_ERR_WORKSPACE;   // beyond the static scratch
     void *scratch = nullptr;
     const pa_status_t st = scratch_on_current_device(&scratch);

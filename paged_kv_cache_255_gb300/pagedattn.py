@@ -36,6 +36,7 @@ SIGNATURES = {
                     _I32, _I64, _P], _I32),
     "pa_take_device_error": ([_P, _P], _I32),
     "pa_debug_prefill_fault": ([_I32], _I32),
+    "pa_debug_kernel_variant": ([_I32], _I32),
     "pa_prefill_layout": ([_P, _P, _P, _P, _I32, _P, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32,
                            _I32, _I32, _I64, _I32, _P], _I32),
     "pa_store_kvcache_layout": ([_P, _P, _P, _P, _P, _I64, _I32, _I32, _I32, _I64, _I32, _P],
@@ -313,6 +314,16 @@ def debug_prefill_fault(mode: int) -> None:
     one barrier arrival so that a bounded wait runs out and code 2 is recorded;
     mode 0 turns it off."""
     _check("pa_debug_prefill_fault", lib().pa_debug_prefill_fault(int(mode)))
+
+
+VARIANT_DECODE_SIMT, VARIANT_PREFILL_MMA = 1, 2
+
+
+def debug_kernel_variant(flags: int) -> None:
+    """Test hook (off by default): run the comparison kernels kept for tests
+    (VARIANT_DECODE_SIMT: CUDA-core decode tiles; VARIANT_PREFILL_MMA: the
+    mma.sync prefill kernel) instead of the product kernels; 0 restores them."""
+    _check("pa_debug_kernel_variant", lib().pa_debug_kernel_variant(int(flags)))
 
 
 class DecodeStepGraph:

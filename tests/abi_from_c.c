@@ -49,6 +49,7 @@ int main(void)
         pa_prefill_layout;
     pa_status_t (*take_error)(int32_t *, void *) = pa_take_device_error;
     pa_status_t (*fault_hook)(int) = pa_debug_prefill_fault;
+    pa_status_t (*variant_hook)(int) = pa_debug_kernel_variant;
     int failures = 0;
 
     if (strcmp(status_name(PA_ERR_WORKSPACE), "PA_ERR_WORKSPACE") != 0)
@@ -83,6 +84,24 @@ int main(void)
         ++failures;
     if (noalloc(NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 2, 16, 8, 64, 16, 10, NULL) !=
         PA_ERR_UNSUPPORTED)
+        ++failures;
+    /* pa_decode_noalloc answers like pa_decode: an empty batch is PA_OK with
+     * no device (this program runs with none visible), bad head counts are
+     * argument errors */
+    if (noalloc(NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 0, 16, 8, 128, 16, 10, NULL) != PA_OK)
+        ++failures;
+    if (noalloc(NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 0, 64, 4, 128, 16, 10, NULL) != PA_OK)
+        ++failures;
+    if (noalloc(NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 2, 12, 8, 128, 16, 10, NULL) !=
+        PA_ERR_INVALID_ARG)
+        ++failures;
+    if (noalloc(NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 2, 0, 8, 128, 16, 10, NULL) !=
+        PA_ERR_INVALID_ARG)
+        ++failures;
+    if (noalloc(NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 2, 16, 8, 128, 16, 10, NULL) !=
+        PA_ERR_INVALID_ARG)
+        ++failures;
+    if (variant_hook(4) != PA_ERR_INVALID_ARG || variant_hook(0) != PA_OK)
         ++failures;
     if (decode_layout(NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 2, 16, 8, 128, 16, 10,
                       (pa_layout_t)3, NULL, 0, 0, NULL) != PA_ERR_INVALID_ARG)

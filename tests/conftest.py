@@ -28,3 +28,13 @@ def pa_lib():
     from paged_kv_cache_255_gb300 import build, pagedattn
     build.build()
     return pagedattn.lib()
+
+
+@pytest.fixture(autouse=True)
+def _product_kernels_after_each_test():
+    """Tests that select a comparison kernel (pa_debug_kernel_variant) leave
+    the product kernels selected for the next test."""
+    yield
+    from paged_kv_cache_255_gb300 import pagedattn
+    if pagedattn._lib is not None:
+        pagedattn.debug_kernel_variant(0)

@@ -67,7 +67,7 @@ def _decode_case(seed):
 
 @pytest.mark.parametrize("kernel", ["mma", "simt"])
 def test_decode_reads_out_of_range_block_as_zeros_and_reports(kernel, monkeypatch):
-    monkeypatch.setenv("PA_DECODE_KERNEL", kernel)
+    gu.decode_kernel(kernel)
     wl, s, nb = _decode_case(9)
     bt = wl.block_tables.copy()
     bt[s, 1] = wl.num_blocks + 11                        # a live entry, outside the pool
@@ -100,7 +100,7 @@ def test_decode_never_reads_entries_past_the_last_block():
 
 @pytest.mark.parametrize("kernel", ["tc", "mma"])
 def test_prefill_reads_out_of_range_block_as_zeros_and_reports(kernel, monkeypatch):
-    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
+    gu.prefill_kernel(kernel)
     spec = inputs.Spec("bad_pf", ((1, 1, 1),), 16, 8, 16, store_mode="none")
     pb = inputs.prefill_batch(spec, seed=3, context_lens=[300, 90], chunk_lens=[100, 90])
     O = oracle.get()

@@ -40,7 +40,7 @@ KERNELS = ["mma", "simt"]
 
 @pytest.fixture(params=KERNELS)
 def kernel(request, monkeypatch):
-    monkeypatch.setenv("PA_DECODE_KERNEL", request.param)
+    gu.decode_kernel(request.param)
     return request.param
 
 
@@ -130,12 +130,15 @@ FULL = ["qwen3_0_6b", "qwen3_0_6b_bs256", "large_batch", "long_context", "prefix
 
 
 def _sample_pairs(wl, n, seed):
+    """Every query head of the 8 longest sequences (on long_context these are
+    the units the split-K path cuts into the most pieces), the first and last
+    output, and random (sequence, head) pairs up to n more."""
     rng = np.random.Generator(np.random.PCG64(seed))
     S, Hq = wl.num_seqs, wl.spec.num_q_heads
-    longest = np.argsort(-wl.context_lens)[:8]
-    pairs = [(int(s), int(rng.integers(Hq))) for s in longest]
+    longest = np.argsort(-wl.context_lens, kind="stable")[:8]
+    pairs = [(int(s), h) for s in longest for h in range(Hq)]
     pairs += [(0, 0), (S - 1, Hq - 1)]
-    while len(pairs) < n:
+    for _ in range(n):
         pairs.append((int(rng.integers(S)), int(rng.integers(Hq))))
     return np.array(pairs, dtype=np.int32)
 
@@ -151,7 +154,7 @@ def test_full_size_sampled(name):
         assert np.array_equal(gu.host_bits(gkc), kc) and np.array_equal(gu.host_bits(gvc), vc)
     else:
         kc, vc = host_k, host_v
-    pairs = _sample_pairs(wl, 48, seed=1)
+    pairs = _sample_pairs(wl, 40, seed=1)
     ref = O.decode_pairs(wl.q.cpu(), kc, vc, wl.block_tables, wl.context_lens, wl.scale, pairs)
     got = out[torch.from_numpy(pairs[:, 0]).long(), torch.from_numpy(pairs[:, 1]).long()]
     gu.assert_close(got, ref, name)

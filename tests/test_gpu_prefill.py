@@ -100,7 +100,7 @@ KERNELS = ["tc", "mma"]
 @pytest.mark.parametrize("kernel", KERNELS)
 @pytest.mark.parametrize("name,spec,chunk,lens,chunks", CASES, ids=[c[0] for c in CASES])
 def test_prefill_matches_oracle(name, spec, chunk, lens, chunks, kernel, monkeypatch):
-    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
+    gu.prefill_kernel(kernel)
     pb = inputs.prefill_batch(spec, seed=61, chunk=chunk, context_lens=lens, chunk_lens=chunks)
     kc, vc = _oracle_caches(pb)
     ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
@@ -116,7 +116,7 @@ def test_prefill_matches_oracle(name, spec, chunk, lens, chunks, kernel, monkeyp
 @pytest.mark.parametrize("kernel", KERNELS)
 def test_small_max_query_len_hint_still_correct(kernel, monkeypatch):
     """The hint only sizes the grid: a CTA walks further query tiles itself."""
-    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
+    gu.prefill_kernel(kernel)
     spec = _spec("h", 16, 8, 16)
     pb = inputs.prefill_batch(spec, seed=62, context_lens=[700, 300], chunk_lens=[650, 300])
     d = _device(pb)
@@ -164,7 +164,7 @@ def _sampled_rows_ref(pb, kc, vc, rows):
 def test_negative_and_zero_scale(kernel, scale, monkeypatch):
     """A negative scale flips which score is the max; scale 0 is uniform
     attention over the visible keys (masked keys still get nothing)."""
-    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
+    gu.prefill_kernel(kernel)
     spec = _spec("k", 16, 8, 16)
     pb = inputs.prefill_batch(spec, seed=66, context_lens=[150, 40, 300],
                               chunk_lens=[100, 40, 260])
@@ -241,7 +241,7 @@ def test_random_prefill_steps(case, monkeypatch):
     ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
                                pb.query_start_loc, pb.wl.scale)
     for kernel in KERNELS:
-        monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
+        gu.prefill_kernel(kernel)
         d = _device(pb)
         out = _gpu_step(pb, d)
         gu.assert_close(out, ref, f"random case {case} ({kernel}): g {spec.num_q_heads // spec.num_kv_heads} "
@@ -261,7 +261,7 @@ def test_head_major_pool(name, spec, lens, chunks, kernel, monkeypatch):
     """The step on a head-major pool [NB, Hkv, bs, D] (store and prefill both
     head-major) matches the oracle, and the prefill gives the same bits as on
     the token-major pool holding the same values."""
-    monkeypatch.setenv("PA_PREFILL_KERNEL", kernel)
+    gu.prefill_kernel(kernel)
     pb = inputs.prefill_batch(spec, seed=67, context_lens=lens, chunk_lens=chunks)
     kc, vc = _oracle_caches(pb)
     ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,

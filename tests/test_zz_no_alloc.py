@@ -4,9 +4,11 @@ Such a caller cannot hand pa_decode a workspace (it may not call cudaMalloc
 on its path, or device memory belongs to a framework that only passes in
 inputs and outputs), so this entry point keeps its scratch in a static
 device array inside the library. The test calls it through the C ABI twice
-in a row, on two different decode steps, and checks each output against
-pa_decode's on the same inputs within the parity tolerance; a head
-configuration too big for the static scratch must be refused.
+in a row, on two decode steps with the same head configuration and different
+length mixes (partial results a first call left in the shared array would
+show up in the second), and checks each output bit for bit against
+pa_decode's on the same inputs and element by element against the fp64
+oracle; a head configuration too big for the static scratch must be refused.
 
 Kept in its own file, collected last, so that a run stopping at the first
 failure has already run every other test.
@@ -16,6 +18,7 @@ import ctypes
 import pytest
 import torch
 
+import oracle
 from paged_kv_cache_255_gb300 import inputs
 from paged_kv_cache_255_gb300 import pagedattn as pa
 
@@ -37,11 +40,17 @@ def _noalloc(lib, d, wl):
     return st, out
 
 
-def test_noalloc_matches_decode_on_two_calls(pa_lib):
+def test_noalloc_matches_decode_and_oracle_on_two_calls(pa_lib):
+    # both steps have 32 query / 8 KV heads; the second mixes one long
+    # sequence (cut into many split-K pieces) with short ones
     steps = [inputs.scaled(inputs.SPECS["large_batch"], num_seqs=24, ctx_div=4),
              inputs.scaled(inputs.SPECS["long_context"], num_seqs=16, ctx_div=8)]
+    heads = {(s.num_q_heads, s.num_kv_heads) for s in steps}
+    assert len(heads) == 1
+    O = oracle.get()
     for i, spec in enumerate(steps):
         wl = inputs.generate(spec, seed=40 + i, device="cuda")
+        host_k, host_v = wl.k_cache.cpu(), wl.v_cache.cpu()
         d = gu.device_inputs(wl)
         if wl.slot_mapping.shape[0]:
             pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
@@ -50,8 +59,11 @@ def test_noalloc_matches_decode_on_two_calls(pa_lib):
         st, got = _noalloc(pa_lib, d, wl)
         torch.cuda.synchronize()
         assert st == pa.PA_OK, pa.status_string(st)
-        ref = want.float().cpu().double().numpy()
-        gu.assert_close(got, ref, f"noalloc call {i + 1}")
+        assert torch.equal(got.view(torch.int16), want.view(torch.int16)), \
+            f"noalloc call {i + 1} differs from pa_decode"
+        kc, vc = O.store_kvcache(wl.k_new.cpu(), wl.v_new.cpu(), host_k, host_v, wl.slot_mapping)
+        ref = O.decode(wl.q.cpu(), kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+        gu.assert_close(got, ref, f"noalloc call {i + 1} against the oracle")
 
 
 def test_noalloc_refuses_scratch_beyond_limit(pa_lib):
