@@ -217,6 +217,10 @@ pa_status_t decode_check_args(const void *q, const void *k_cache, const void *v_
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return PA_ERR_INVALID_ARG;
     if (max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_INVALID_ARG;
+    // the tile copies address pool rows with int32 coordinates
+    if (num_blocks * block_size >= ((int64_t)1 << 31) ||
+        num_blocks * num_kv_heads >= ((int64_t)1 << 31))
+        return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 

@@ -15,26 +15,28 @@
 //   * P workers (one warp each, persistent: P = SMs x resident CTAs x warps)
 //     take equal contiguous shares [w W / P, (w + 1) W / P) of that space, so
 //     every SM streams the same number of bytes whatever the length mix.
-//   * A worker streams its tiles through a private kStages-deep cp.async ring
-//     in shared memory (16-byte zero-filling copies; rows past the sequence
-//     end are never read) and keeps, per query head of its KV head's group, an
-//     online softmax (running max in log2 units, running sum) and an fp32
-//     accumulator of P.V.
-//   * A unit that lies wholly in one share is written straight to `out`. A
-//     unit cut by share boundaries leaves one partial (o, m, l) per share in
-//     the workspace; the worker holding its first tile records a combine task,
-//     and the combine kernel merges the pieces by log-sum-exp weights
-//     (split-K / flash-decoding).
+//   * A worker streams its tiles through a private kStages-deep ring in shared
+//     memory. One lane fills a stage with four TMA boxes (the K tile and the
+//     V tile, each 16 rows x 64 head dims twice, 128-byte swizzle) counted
+//     on the stage's mbarrier; every lane then waits on that barrier. A
+//     tile with no tokens, or with a block id outside the pool, is
+//     zero-filled by the warp instead, and the V rows of a sequence's last,
+//     partly used tile are zeroed after they land. Per query head of its KV
+//     head's group the worker keeps an online softmax (running max in log2
+//     units, running sum) and an fp32 accumulator of P.V.
 // Two interchangeable tile computations sit inside the same worker loop:
 //   * MmaTile: q.K^T and P.V on the tensor cores with mma.sync m16n8k16 bf16
 //     (fp32 accumulate): 16 tokens x 8 (or 16) query heads x 128 dims per
 //     tile; the default.
 //   * SimtTile: the same on the CUDA cores, lane l owning dims [4l, 4l + 4).
-// The kernels never wait on one another inside a launch.
+// The kernels never wait on one another inside a launch; a warp waits only on
+// its own copies, and every such wait is bounded (1 s, then the launch records
+// code 2 and the warp exits).
 #include <cmath>
 
 #include "common.cuh"
 #include "kernels.h"
+#include "tcgen05.cuh"
 
 namespace pa {
 
@@ -44,13 +46,57 @@ namespace {
 
 constexpr int kWarps = 4;      // workers per CTA
 // Ring depth: one tile in flight while the warp works on the other. With the
-// ring this shallow, three CTAs fit an SM (12 warps, the register limit), which
-// measured faster than two CTAs of three-stage rings (qwen3-shaped step 43.4 ->
-// 42.3 us, large batch 420 -> 413 us, long context unchanged).
+// ring this shallow, three CTAs fit an SM (12 warps), which measured faster
+// than two CTAs of three-stage rings.
 constexpr int kStages = 2;
+constexpr int kBoxBytes = kTileBytes / 2;     // one TMA box: 16 rows x 128 B (64 head dims)
 constexpr int kStageBytes = 2 * kTileBytes;   // K tile then V tile
+constexpr int kRingBytes = kStages * kStageBytes;
 constexpr int kCombineBatch = 8;              // pieces a combine warp loads at once
 constexpr float kNegInf = -INFINITY;
+constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // bounded waits give up after 1 s
+
+// Byte offset, inside a K or V tile in shared memory, of the 16-byte chunk
+// holding head dims [8c, 8c + 8) of token row r. The tile is two TMA boxes
+// (dims 0-63, then 64-127) of 16 rows x 128 B in the 128-byte swizzle: chunk
+// k of a 128-byte row r sits at position k ^ (r % 8).
+__device__ __forceinline__ uint32_t chunk_off(int r, int c) {
+    return (uint32_t)((c >> 3) * kBoxBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];\n" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
+// The warp waits until the phase of `bar` with the given parity completes.
+// It first polls (every lane tests, a vote answers, __syncwarp orders the
+// lanes that saw the completion before the rest; a suspended waiter would
+// resume late), then lane 0 waits with a time limit. False when the limit
+// ran out.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, int lane) {
+    for (int i = 0; i < 4096; ++i)
+        if (__any_sync(0xffffffffu, tc::mbar_test_wait(bar, parity))) {
+            __syncwarp();
+            return true;
+        }
+    bool ok = true;
+    if (lane == 0) {
+        const uint64_t t0 = tc::globaltimer_ns();
+        while (!tc::mbar_try_wait(bar, parity)) {
+            if (tc::globaltimer_ns() - t0 > kWaitLimitNs) {
+                ok = false;
+                break;
+            }
+        }
+    }
+    ok = __shfl_sync(0xffffffffu, ok ? 1 : 0, 0) != 0;
+    __syncwarp();
+    return ok;
+}
 
 __device__ __forceinline__ int clamp_len(const int32_t *cl, int s, int max_len) {
     int L = __ldg(cl + s);
@@ -92,42 +138,56 @@ __device__ __forceinline__ int tile_block(const Cursor &c, const DecodeArgs &a) 
                  ((c.j << 4) >> a.block_size_log2));
 }
 
-// Issue the cp.async copies of one K tile and one V tile (16 rows x 256 B
-// each) into `stage`. Lane l copies 16-byte chunk (l & 15) of rows
-// (l >> 4) + 2i; each instruction covers two whole 256-byte rows. With
-// SWZ the chunk lands at position chunk ^ (row & 7) of its row, so that the
-// eight rows an ldmatrix reads at one logical chunk fall in eight different
-// bank groups.
-template <bool SWZ>
-__device__ __forceinline__ void issue_tile(const Cursor &c, int bid, uint8_t *stage,
-                                           const DecodeArgs &a, int lane) {
-    int valid = tile_valid(c);
-    if (bid < 0 || (int64_t)bid >= a.num_blocks) {   // never address outside the pool
-        if (valid > 0 && lane == 0) atomicCAS(&g_decode_error, 0, kErrBadBlock);
-        valid = 0;
-    }
-    const int off = (c.j << 4) & ((1 << a.block_size_log2) - 1);
-    // token-major pool [NB][bs][Hkv][D]: a tile's rows are Hkv rows apart;
-    // head-major pool [NB][Hkv][bs][D]: they are one contiguous run
-    const int64_t row0 = a.head_major
-        ? ((((int64_t)bid * a.num_kv_heads + c.kvh) << a.block_size_log2) + off)
-        : ((((int64_t)bid << a.block_size_log2) + off) * a.num_kv_heads + c.kvh);
-    const int64_t rstride = a.head_major ? (int64_t)kRowBytes : (int64_t)a.num_kv_heads * kRowBytes;
-    const char *kb = static_cast<const char *>(a.k_cache) + row0 * kRowBytes;
-    const char *vb = static_cast<const char *>(a.v_cache) + row0 * kRowBytes;
-    const int chunk = lane & 15;
-    const uint32_t dst = smem_u32(stage);
+// Fill `stage` with the K tile and the V tile under cursor c (physical block
+// bid): two TMA boxes each, issued by lane 0 and counted in bytes on `bar`.
+// A tile with no tokens, or whose block id lies outside the pool, is written
+// with zeros by the warp instead (each of its keys then scores 0 and adds a
+// zero value) and `bar` gets a plain arrival. The stage's previous contents
+// must have been read by every lane (the __syncwarp below orders that).
+__device__ __forceinline__ void issue_tile(const Cursor &c, int bid, uint8_t *stage, uint32_t bar,
+                                           const DecodeArgs &a, const CUtensorMap *mk,
+                                           const CUtensorMap *mv, int lane) {
+    const int valid = tile_valid(c);
+    const bool bad = bid < 0 || (int64_t)bid >= a.num_blocks;   // never address outside the pool
+    if (valid > 0 && bad && lane == 0) atomicCAS(&g_decode_error, 0, kErrBadBlock);
+    __syncwarp();
+    if (valid > 0 && !bad) {
+        if (lane == 0) {
+            // token-major pool: (x, KV head, block * bs + offset); head-major
+            // pool: (x, offset, block * Hkv + KV head)
+            const int off = (c.j << 4) & ((1 << a.block_size_log2) - 1);
+            const int c1 = a.head_major ? off : c.kvh;
+            const int c2 = a.head_major ? bid * a.num_kv_heads + c.kvh
+                                        : (bid << a.block_size_log2) + off;
+            const uint32_t dst = smem_u32(stage);
+            mbar_arrive_expect_tx(bar, kStageBytes);
+            tc::tma_load_3d(dst, mk, 0, c1, c2, bar);
+            tc::tma_load_3d(dst + kBoxBytes, mk, 64, c1, c2, bar);
+            tc::tma_load_3d(dst + kTileBytes, mv, 0, c1, c2, bar);
+            tc::tma_load_3d(dst + kTileBytes + kBoxBytes, mv, 64, c1, c2, bar);
+        }
+    } else {
+        uint4 *z = reinterpret_cast<uint4 *>(stage);
 #pragma unroll
-    for (int i = 0; i < 8; ++i) {
-        const int r = (lane >> 4) + 2 * i;
-        const bool ok = r < valid;
-        const int64_t o = ok ? r * rstride + chunk * 16 : 0;
-        const int pos = SWZ ? (chunk ^ (r & 7)) : chunk;
-        cp_async_16(dst + r * kRowBytes + pos * 16,
-                    ok ? kb + o : static_cast<const char *>(a.k_cache), ok ? 16 : 0);
-        cp_async_16(dst + kTileBytes + r * kRowBytes + pos * 16,
-                    ok ? vb + o : static_cast<const char *>(a.v_cache), ok ? 16 : 0);
+        for (int i = 0; i < kStageBytes / 16 / 32; ++i) z[i * 32 + lane] = make_uint4(0u, 0u, 0u, 0u);
+        tc::fence_proxy_async();    // a later TMA into this stage lands after these stores
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bar);
     }
+}
+
+// Zero rows [valid, 16) of a V tile that has landed: keys past the sequence
+// end get zero weight, but 0 x NaN would still be NaN. Chunk i of the tile is
+// box i / 128, row (i / 8) % 16.
+__device__ __forceinline__ void zero_v_tail(uint8_t *vtile, int valid, int lane) {
+    uint4 *z = reinterpret_cast<uint4 *>(vtile);
+#pragma unroll
+    for (int k = 0; k < kTileBytes / 16 / 32; ++k) {
+        const int i = k * 32 + lane;
+        if (((i >> 3) & 15) >= valid) z[i] = make_uint4(0u, 0u, 0u, 0u);
+    }
+    tc::fence_proxy_async();
+    __syncwarp();
 }
 
 // Element offset of the q (and out) row of column c of a (sequence, KV head)
@@ -150,7 +210,7 @@ __device__ __forceinline__ int col_limit(const DecodeArgs &a, int L, int c) {
 // Tile computation on the tensor cores.
 //
 // Scores as S^T = K Q^T: A = the K tile (16 tokens x 16 dims per k-step,
-// ldmatrix from the swizzled ring), B = Q^T (16 dims x 8 heads, kept in
+// ldmatrix from the swizzled stage), B = Q^T (16 dims x 8 heads, kept in
 // registers for the unit), C = 16 tokens x 8 heads in fp32. Lane (gid =
 // lane / 4, tig = lane % 4) holds tokens gid and gid + 8 of heads 2 tig and
 // 2 tig + 1, so the per-head max over tokens is a 3-step xor reduction.
@@ -160,7 +220,6 @@ __device__ __forceinline__ int col_limit(const DecodeArgs &a, int L, int c) {
 template <int GP>
 struct MmaTile {
     static constexpr int NT = GP > 8 ? 2 : 1;      // 8-head column tiles
-    static constexpr bool kSwizzle = true;
     static constexpr int kScratchFloats = 0;
     uint32_t qb[NT][8][2];
     float o[NT][8][4];
@@ -207,11 +266,12 @@ struct MmaTile {
         for (int nt = 0; nt < NT; ++nt)
 #pragma unroll
             for (int i = 0; i < 4; ++i) s[nt][i] = 0.f;
-        const uint32_t krow = base + (i7 + 8 * (mi & 1)) * kRowBytes;
+        // lane supplies row i7 + 8 (mi & 1), dim chunk 2 kk + (mi >> 1) of the K tile
+        const uint32_t krow = base + (i7 + 8 * (mi & 1)) * 128;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
             uint32_t a[4];
-            ldmatrix_x4(krow + (((2 * kk + (mi >> 1)) ^ i7) << 4), a);
+            ldmatrix_x4(krow + (kk >> 2) * kBoxBytes + ((((2 * kk + (mi >> 1)) & 7) ^ i7) << 4), a);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(s[nt], a, qb[nt][kk][0], qb[nt][kk][1]);
         }
@@ -233,7 +293,9 @@ struct MmaTile {
             }
             const float mn0 = fmaxf(m[nt][0], mx0), mn1 = fmaxf(m[nt][1], mx1);
             const float ms0 = mn0 == kNegInf ? 0.f : mn0, ms1 = mn1 == kNegInf ? 0.f : mn1;
-            const float al0 = ex2(m[nt][0] - ms0), al1 = ex2(m[nt][1] - ms1);
+            // a column whose running max did not move keeps its scale exactly
+            const float al0 = mn0 == m[nt][0] ? 1.f : ex2(m[nt][0] - ms0);
+            const float al1 = mn1 == m[nt][1] ? 1.f : ex2(m[nt][1] - ms1);
             const uint32_t w0 = pack_bf16x2(ex2(s0 - ms0), ex2(s1 - ms1));   // token gid
             const uint32_t w1 = pack_bf16x2(ex2(s2 - ms0), ex2(s3 - ms1));   // token gid + 8
             // the running sum adds the same bf16-rounded weights the tensor cores use
@@ -243,20 +305,25 @@ struct MmaTile {
             m[nt][1] = mn1;
             pb0[nt] = movmatrix_trans(w0);
             pb1[nt] = movmatrix_trans(w1);
+            // rescale the accumulators only when some column's max moved
+            // (rare once a long sequence's first tiles have been seen)
+            if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) {
-                o[nt][mt][0] *= al0;
-                o[nt][mt][1] *= al1;
-                o[nt][mt][2] *= al0;
-                o[nt][mt][3] *= al1;
+                for (int mt = 0; mt < 8; ++mt) {
+                    o[nt][mt][0] *= al0;
+                    o[nt][mt][1] *= al1;
+                    o[nt][mt][2] *= al0;
+                    o[nt][mt][3] *= al1;
+                }
             }
         }
 
-        const uint32_t vrow = base + kTileBytes + (i7 + 8 * (mi >> 1)) * kRowBytes;
+        // lane supplies row i7 + 8 (mi >> 1), dim chunk 2 mt + (mi & 1) of the V tile
+        const uint32_t vrow = base + kTileBytes + (i7 + 8 * (mi >> 1)) * 128;
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             uint32_t a[4];
-            ldmatrix_x4_trans(vrow + (((2 * mt + (mi & 1)) ^ i7) << 4), a);
+            ldmatrix_x4_trans(vrow + (mt >> 2) * kBoxBytes + ((((2 * mt + (mi & 1)) & 7) ^ i7) << 4), a);
 #pragma unroll
             for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[nt][mt], a, pb0[nt], pb1[nt]);
         }
@@ -341,7 +408,6 @@ __device__ __forceinline__ void butterfly_sum(float (&v)[NV], int lane) {
 template <int GP>
 struct SimtTile {
     static constexpr int HP = GP >= 2 ? GP / 2 : 1;     // heads whose scores a lane holds
-    static constexpr bool kSwizzle = false;
     static constexpr int kScratchFloats = 16 * GP + GP;  // p[16][GP], alpha[GP]
     float qf[GP][4], o[GP][4], m_run[HP], l_run[HP];
     int L_;             // tokens of the unit's sequence (one query token per sequence)
@@ -379,9 +445,11 @@ struct SimtTile {
         const int hb = GP >= 2 ? (lane & 1) * HP : 0;
 
         float part[16 * GP];
+        // lane l reads dims [4l, 4l + 4): half of 16-byte chunk l / 2 of each row
+        const uint32_t lane_half = (lane & 1) * 8;
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(sk + t * kRowBytes + lane * 8);
+            const uint2 u = *reinterpret_cast<const uint2 *>(sk + chunk_off(t, lane >> 1) + lane_half);
             const float k0 = bf16_lo(u.x), k1 = bf16_hi(u.x), k2 = bf16_lo(u.y), k3 = bf16_hi(u.y);
 #pragma unroll
             for (int h = 0; h < GP; ++h)
@@ -415,7 +483,7 @@ struct SimtTile {
         }
 #pragma unroll
         for (int t = 0; t < 16; ++t) {
-            const uint2 u = *reinterpret_cast<const uint2 *>(sv + t * kRowBytes + lane * 8);
+            const uint2 u = *reinterpret_cast<const uint2 *>(sv + chunk_off(t, lane >> 1) + lane_half);
             const float v0 = bf16_lo(u.x), v1 = bf16_hi(u.x), v2 = bf16_lo(u.y), v3 = bf16_hi(u.y);
 #pragma unroll
             for (int h = 0; h < GP; ++h) {
@@ -451,12 +519,14 @@ struct SimtTile {
     }
 };
 
-// Per-warp shared memory: the ring, then the tile scratch, then m/l per head.
+// Shared memory of a CTA, from a 1024-byte aligned start (the 128-byte swizzle
+// of the TMA boxes repeats every 1024 bytes): every warp's ring, then per warp
+// its stage barriers, the tile scratch and m / l per head.
 template <class Tile, int GP>
 struct Layout {
     static constexpr int kSmallFloats = Tile::kScratchFloats + 2 * GP;
-    static constexpr int kWarpBytes = kStages * kStageBytes + ((kSmallFloats * 4 + 127) / 128) * 128;
-    static constexpr int kCtaBytes = kWarps * kWarpBytes;
+    static constexpr int kSmallBytes = ((8 * kStages + kSmallFloats * 4 + 127) / 128) * 128;
+    static constexpr int kCtaBytes = 1024 + kWarps * (kRingBytes + kSmallBytes);   // + alignment slack
 };
 
 // CTA prologue: the total tile count W, the share count actually used, and
@@ -553,14 +623,24 @@ __device__ __forceinline__ void prefetch_inputs(const DecodeArgs &a) {
 
 template <class Tile, int GP>
 __global__ void __launch_bounds__(kWarps * 32)
-decode_kernel(const DecodeArgs a) {
+decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
+              const __grid_constant__ CUtensorMap tmap_v) {
     using Lay = Layout<Tile, GP>;
-    extern __shared__ __align__(128) uint8_t smem[];
+    extern __shared__ uint8_t smem_raw[];
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    uint8_t *ring = smem + warp * Lay::kWarpBytes;
-    float *scratch = reinterpret_cast<float *>(ring + kStages * kStageBytes);
+    uint8_t *smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+    uint8_t *ring = smem + warp * kRingBytes;
+    uint8_t *small = smem + kWarps * kRingBytes + warp * Lay::kSmallBytes;
+    const uint32_t bar0 = smem_u32(small);                      // kStages mbarriers
+    float *scratch = reinterpret_cast<float *>(small + 8 * kStages);
     float *sm_m = scratch + Tile::kScratchFloats;
     float *sm_l = sm_m + GP;
+    if (lane == 0) {
+#pragma unroll
+        for (int i = 0; i < kStages; ++i) tc::mbar_init(bar0 + 8 * i, 1);
+        tc::fence_mbar_init();
+    }
+    __syncwarp();
 
     // Launched as a programmatic dependent of the previous kernel in the
     // stream (normally the store of this step's K/V rows). While that kernel
@@ -587,6 +667,8 @@ decode_kernel(const DecodeArgs a) {
     }
 
     uint32_t *outg = static_cast<uint32_t *>(a.out);
+    uint32_t phase = 0;      // bit i: parity of stage i's next barrier phase
+    uint32_t pending = 0;    // bit i: stage i has been filled and not yet waited for
 
     // producer: runs kStages - 1 tiles ahead of the consumer
     Cursor pc = cc;
@@ -596,12 +678,13 @@ decode_kernel(const DecodeArgs a) {
 #pragma unroll
     for (int i = 0; i < kStages - 1; ++i) {
         if (Tp < T1) {
-            issue_tile<Tile::kSwizzle>(pc, p_bid, ring + stage_p * kStageBytes, a, lane);
+            issue_tile(pc, p_bid, ring + stage_p * kStageBytes, bar0 + 8 * stage_p, a, &tmap_k,
+                       &tmap_v, lane);
+            pending |= 1u << stage_p;
             cursor_advance(pc, a, max_len);
             ++Tp;
             p_bid = Tp < T1 ? tile_block(pc, a) : 0;
         }
-        cp_async_commit();
         stage_p = stage_p + 1 == kStages ? 0 : stage_p + 1;
     }
 
@@ -612,15 +695,17 @@ decode_kernel(const DecodeArgs a) {
     int64_t piece_T = T0;       // flat index of the piece's first tile
     int piece_j0 = 0;
     int4 task = make_int4(-1, 0, 0, 0);
+    bool failed = false;
 
     for (int64_t T = T0; T < T1; ++T) {
         if (Tp < T1) {
-            issue_tile<Tile::kSwizzle>(pc, p_bid, ring + stage_p * kStageBytes, a, lane);
+            issue_tile(pc, p_bid, ring + stage_p * kStageBytes, bar0 + 8 * stage_p, a, &tmap_k,
+                       &tmap_v, lane);
+            pending |= 1u << stage_p;
             cursor_advance(pc, a, max_len);
             ++Tp;
             p_bid = Tp < T1 ? tile_block(pc, a) : 0;
         }
-        cp_async_commit();
         stage_p = stage_p + 1 == kStages ? 0 : stage_p + 1;
 
         if (fresh) {
@@ -630,9 +715,15 @@ decode_kernel(const DecodeArgs a) {
             tl.begin(a, cc, lane);
         }
 
-        cp_async_wait<kStages - 1>();
-        __syncwarp();
+        if (!warp_wait(bar0 + 8 * stage_c, (phase >> stage_c) & 1u, lane)) {
+            failed = true;
+            break;
+        }
+        phase ^= 1u << stage_c;
+        pending &= ~(1u << stage_c);
         uint8_t *stage = ring + stage_c * kStageBytes;
+        const int valid = tile_valid(cc);
+        if (valid > 0 && valid < 16) zero_v_tail(stage + kTileBytes, valid, lane);
         tl.tile(stage, cc.j << 4, a.scale_log2, scratch, lane);
         stage_c = stage_c + 1 == kStages ? 0 : stage_c + 1;
 
@@ -643,6 +734,7 @@ decode_kernel(const DecodeArgs a) {
             float oc[GP][4];
             __syncwarp();
             tl.finish(reinterpret_cast<float *>(stage), sm_m, sm_l, oc, lane);
+            tc::fence_proxy_async();     // the TMA that refills the stage lands after these stores
             __syncwarp();
             if (piece_j0 == 0 && unit_end) {
                 // the whole unit is in this share: normalise and write bf16
@@ -681,7 +773,15 @@ decode_kernel(const DecodeArgs a) {
         }
         cursor_advance(cc, a, max_len);
     }
-    cp_async_wait<0>();
+    if (failed) {
+        // a copy did not land in time: record it, give the copies still in
+        // flight into this warp's ring a bounded chance to land, own no
+        // combine task, and stop (the launch's outputs are undefined)
+        if (lane == 0) atomicCAS(&g_decode_error, 0, kErrTimeout);
+        for (int i = 0; i < kStages; ++i)
+            if ((pending >> i) & 1u && i != stage_c) warp_wait(bar0 + 8 * i, (phase >> i) & 1u, lane);
+        task = make_int4(-1, 0, 0, 0);
+    }
     if (lane == 0) a.tasks[w] = task;
 }
 
@@ -760,7 +860,7 @@ struct Launcher {
     // scheduled while the kernel before it in the stream is still running, and
     // waits for it (griddepcontrol.wait) before touching its results.
     static cudaError_t launch_pdl(const void *fn, dim3 grid, unsigned block, size_t smem,
-                                  const DecodeArgs &a, cudaStream_t st) {
+                                  void **args, cudaStream_t st) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = grid;
         cfg.blockDim = dim3(block);
@@ -771,18 +871,25 @@ struct Launcher {
         attr[0].val.programmaticStreamSerializationAllowed = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        void *args[] = {const_cast<DecodeArgs *>(&a)};
         return cudaLaunchKernelExC(&cfg, fn, args);
     }
     static cudaError_t launch(const DecodeArgs &a, cudaStream_t st) {
         cudaError_t e = prepare();
         if (e != cudaSuccess) return e;
+        CUtensorMap mk, mv;
+        const int bs = 1 << a.block_size_log2;
+        if (!make_pool_map(&mk, a.k_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0) ||
+            !make_pool_map(&mv, a.v_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0))
+            return cudaErrorInvalidValue;
         const unsigned grid = (a.num_workers + kWarps - 1) / kWarps;
+        DecodeArgs args_copy = a;
+        void *dargs[] = {&args_copy, &mk, &mv};
         e = launch_pdl(reinterpret_cast<const void *>(&decode_kernel<Tile, GP>), dim3(grid),
-                       kWarps * 32, Lay::kCtaBytes, a, st);
+                       kWarps * 32, Lay::kCtaBytes, dargs, st);
         if (e != cudaSuccess) return e;
+        void *cargs[] = {&args_copy};
         e = launch_pdl(reinterpret_cast<const void *>(&combine_kernel<GP>),
-                       dim3((a.num_workers + 3) / 4, a.cols), 128, 0, a, st);
+                       dim3((a.num_workers + 3) / 4, a.cols), 128, 0, cargs, st);
         if (e != cudaSuccess) return e;
         return cudaGetLastError();
     }

@@ -3,6 +3,8 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include "../../include/pagedattn.h"
@@ -108,6 +110,16 @@ cudaError_t take_prefill_error(cudaStream_t stream, int *code);
 cudaError_t take_prefill_mma_error(cudaStream_t stream, int *code);
 cudaError_t take_decode_error(cudaStream_t stream, int *code);
 cudaError_t take_store_error(cudaStream_t stream, int *code);
+
+// cuTensorMapEncodeTiled from the driver (nullptr if unavailable).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
+
+// TMA tensor map over a K or V pool (either layout) whose box is one 16-token
+// tile of one KV head, 64 head dims wide, 128-byte swizzle; two boxes (x = 0
+// and x = 64) make a whole tile. Coordinates: token-major (x, KV head,
+// block * bs + offset); head-major (x, offset, block * Hkv + KV head).
+bool make_pool_map(CUtensorMap *m, const void *pool, int64_t num_blocks, int block_size,
+                   int num_kv_heads, bool head_major);
 
 cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
                                  const int64_t *slot_mapping, int64_t num_tokens,

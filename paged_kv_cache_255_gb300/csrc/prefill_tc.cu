@@ -753,44 +753,11 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void *p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
-                                             &q) == cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// The pool as a 3-D tensor of bf16 with boxes of 16 tokens x 64 dims of one
-// head, 128-byte swizzle: token-major [NB, bs, Hkv, 128] as (128, Hkv, NB * bs)
-// with box (64, 1, 16); head-major [NB, Hkv, bs, 128] as (128, bs, NB * Hkv)
-// with box (64, 16, 1). Either box lands as 16 rows of 128 bytes.
-bool make_pool_map(CUtensorMap *m, const void *pool, int64_t num_blocks, int block_size,
-                   int num_kv_heads, bool head_major) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
-    if (!enc) return false;
-    const cuuint64_t d1 = head_major ? block_size : num_kv_heads;
-    const cuuint64_t d2 = head_major ? num_blocks * num_kv_heads : num_blocks * block_size;
-    const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, d1, d2};
-    const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, d1 * kRowBytes};
-    const cuuint32_t box[3] = {64, head_major ? (cuuint32_t)kGroup : 1u, head_major ? 1u : (cuuint32_t)kGroup};
-    const cuuint32_t estr[3] = {1, 1, 1};
-    return enc(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void *>(pool), dims, strides, box,
-               estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // q [total_q, Hq, 128] bf16 as a 3-D tensor (128, Hq, total_q) with boxes of
 // 64 dims x G heads x 128 / G tokens, 128-byte swizzle: one box is one half
 // (64 dims) of a 128-row query tile.
 bool make_q_map(CUtensorMap *m, const void *q, int total_q, int num_q_heads, int G) {
-    PFN_cuTensorMapEncodeTiled_v12000 enc = encode_fn();
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
     if (!enc) return false;
     const cuuint64_t dims[3] = {(cuuint64_t)kHeadDim, (cuuint64_t)num_q_heads, (cuuint64_t)total_q};
     const cuuint64_t strides[2] = {(cuuint64_t)kRowBytes, (cuuint64_t)num_q_heads * kRowBytes};
