@@ -375,9 +375,18 @@ class DecodeStep:
         return self.pa.decode(q, self.k_cache, self.v_cache, bt, cl, self.wl.scale, out=self.out,
                               workspace=self.ws, head_major=self.HM)
 
-    def step(self):
-        self.store()
-        self.decode()
+    def step(self, kn=None, vn=None, sl=None, q=None, bt=None, cl=None):
+        """Store + decode in one call (pa_decode_step; decode alone when the
+        step stores nothing)."""
+        if not self.has_store or self.Q > 1:
+            self.store(kn, vn, sl)
+            return self.decode(q, bt, cl)
+        return self.pa.decode_step(self.k_new if kn is None else kn,
+                                   self.v_new if vn is None else vn,
+                                   self.slots if sl is None else sl, self.q if q is None else q,
+                                   self.k_cache, self.v_cache, self.bt if bt is None else bt,
+                                   self.cl if cl is None else cl, self.wl.scale, out=self.out,
+                                   workspace=self.ws, head_major=self.HM)
 
     def launches_per_step(self):
         return 3 if self.has_store else 2
@@ -385,8 +394,9 @@ class DecodeStep:
 
 def time_decode(st: DecodeStep, flush, stream, steps, warmup, world):
     """Store + decode per step with the L2 flushed before each step: one pass
-    back to back (the step time) and one with an event between the two calls
-    (the split). Returns milliseconds (max over ranks) and the step times."""
+    through the one-call step (the step time) and one with an event between
+    separate store and decode calls (the split). Returns milliseconds (max
+    over ranks) and the step times."""
     for _ in range(warmup):
         flush.zero_()
         st.step()
@@ -513,8 +523,7 @@ def run_gpu(args, rank, world, local):
 
     def e2e_step():
         d_stage.copy_(h_stage, non_blocking=True)
-        st.store(dk, dv, ds)
-        st.decode(dq, dbt, dcl)
+        st.step(dk, dv, ds, dq, dbt, dcl)
         hout.copy_(st.out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -606,9 +615,9 @@ def run_gpu(args, rank, world, local):
                   "note": "store + decode (and, for e2e, the H2D and D2H copies) captured "
                           "in one CUDA graph, one replay per step"},
         "gpu_launches": launches,
-        "timing": "value: store + decode back to back per step; store_us / decode_us: a "
-                  "second pass with an event between the two calls; workloads: the same "
-                  "two passes on each other step",
+        "timing": "value: one pa_decode_step call (store, then decode) per step; store_us / "
+                  "decode_us: a second pass with separate store and decode calls and an event "
+                  "between them; workloads: the same two passes on each other step",
         "clocks": clk,
         "workloads": subs,
     }

@@ -263,6 +263,37 @@ PA_API pa_status_t pa_decode_multi_layout(const void *q, const void *k_cache, co
                                           size_t workspace_bytes, void *stream);
 
 /*
+ * One decode step in one call: the store of the step's new K/V rows
+ * (pa_store_kvcache_layout with k, v, slot_mapping, num_tokens), then
+ * single-token decode attention over the updated cache (pa_decode_layout
+ * with num_partitions = 0), on `stream`. This is how the engine the pages
+ * describe runs a decode step: the token just projected is written into its
+ * sequence's block, then attention reads the whole sequence back through the
+ * block table ("A vLLM engine small enough to read in one sitting": paged KV
+ * cache management and paged attention for decoding).
+ *
+ * The results are exactly those of the two calls made one after the other.
+ * What the single call adds: the decode kernel's only predecessor is then
+ * this store, which writes the caches and nothing else, so the decode plans
+ * its split of the work (from context_lens) while the store still runs and
+ * waits for the store only before its first cache read. context_lens,
+ * block_tables and q must therefore not overlap k_cache or v_cache.
+ *
+ * Every argument of both parts is checked before anything is launched; the
+ * statuses are those of the two calls (the store's checks first). With
+ * num_tokens == 0 only the decode runs; with num_seqs == 0 only the store.
+ * The workspace is pa_decode's (pa_decode_workspace_size(..., 0)).
+ */
+PA_API pa_status_t pa_decode_step(const void *k, const void *v, const int64_t *slot_mapping,
+                                  int64_t num_tokens, const void *q, void *k_cache,
+                                  void *v_cache, const int32_t *block_tables,
+                                  int max_blocks_per_seq, const int32_t *context_lens,
+                                  float scale, void *out, int num_seqs, int num_q_heads,
+                                  int num_kv_heads, int head_dim, int block_size,
+                                  int64_t num_blocks, pa_layout_t layout, void *workspace,
+                                  size_t workspace_bytes, void *stream);
+
+/*
  * Paged prefill (chunked prefill): a chunk of new tokens per sequence attends
  * causally to the sequence's tokens in the paged cache, as in the engine's
  * prefill phase ("A vLLM engine small enough to read in one sitting": prefill

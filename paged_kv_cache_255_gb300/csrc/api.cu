@@ -78,7 +78,8 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
                         const int32_t *context_lens, int q_len, float scale, void *out,
                         int num_seqs, int num_q_heads, int num_kv_heads, int head_dim,
                         int block_size, int64_t num_blocks, int layout, void *workspace,
-                        size_t workspace_bytes, int num_partitions, void *stream) {
+                        size_t workspace_bytes, int num_partitions, void *stream,
+                        bool plan_early = false) {
     bool nothing_to_do = false;
     const pa_status_t chk = pa::decode_check_args(
         q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, q_len, scale, out,
@@ -114,6 +115,7 @@ pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
     a.scale_log2 = (float)((double)scale * 1.4426950408889634);   // scale * log2(e)
     a.num_workers = P;
     a.min_tiles = num_partitions > 0 ? 1 : pa::kDefaultMinTiles;
+    a.plan_early = plan_early ? 1 : 0;
     pa::decode_carve_workspace(a, workspace, gp);
     const cudaError_t e = pa::launch_decode(a, gp, kind, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? PA_OK : PA_ERR_CUDA;
@@ -123,13 +125,11 @@ pa_status_t store_impl(const void *k, const void *v, void *k_cache, void *v_cach
                        const int64_t *slot_mapping, int64_t num_tokens, int num_kv_heads,
                        int head_dim, int block_size, int64_t num_blocks, int layout,
                        void *stream) {
-    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
-    if (layout != PA_LAYOUT_TOKEN_MAJOR && layout != PA_LAYOUT_HEAD_MAJOR) return PA_ERR_INVALID_ARG;
-    if (head_dim != pa::kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
-    if (num_tokens == 0) return PA_OK;
-    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
-    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
-        return PA_ERR_INVALID_ARG;
+    bool nothing_to_do = false;
+    const pa_status_t chk = pa::store_check_args(k, v, k_cache, v_cache, slot_mapping, num_tokens,
+                                                 num_kv_heads, head_dim, block_size, num_blocks,
+                                                 layout, &nothing_to_do);
+    if (chk != PA_OK || nothing_to_do) return chk;
     const int sms = current_sm_count();
     if (sms <= 0) return PA_ERR_CUDA;
     const cudaError_t e = pa::launch_store_kvcache(
@@ -191,6 +191,24 @@ pa_status_t prefill_impl(const void *q, const void *k_cache, const void *v_cache
 }  // namespace
 
 namespace pa {
+
+pa_status_t store_check_args(const void *k, const void *v, const void *k_cache,
+                             const void *v_cache, const int64_t *slot_mapping, int64_t num_tokens,
+                             int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                             int layout, bool *nothing_to_do) {
+    *nothing_to_do = false;
+    if (num_tokens < 0 || num_kv_heads <= 0 || num_blocks < 0) return PA_ERR_INVALID_ARG;
+    if (layout != PA_LAYOUT_TOKEN_MAJOR && layout != PA_LAYOUT_HEAD_MAJOR) return PA_ERR_INVALID_ARG;
+    if (head_dim != kHeadDimPublic || !block_size_ok(block_size)) return PA_ERR_UNSUPPORTED;
+    if (num_tokens == 0) {
+        *nothing_to_do = true;
+        return PA_OK;
+    }
+    if (!k || !v || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+    if (!aligned16(k) || !aligned16(v) || !aligned16(k_cache) || !aligned16(v_cache))
+        return PA_ERR_INVALID_ARG;
+    return PA_OK;
+}
 
 pa_status_t decode_check_args(const void *q, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int max_blocks_per_seq,
@@ -346,6 +364,41 @@ pa_status_t pa_decode_multi_layout(const void *q, const void *k_cache, const voi
     return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                        q_len, scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim,
                        block_size, num_blocks, layout, workspace, workspace_bytes, 0, stream);
+}
+
+pa_status_t pa_decode_step(const void *k, const void *v, const int64_t *slot_mapping,
+                           int64_t num_tokens, const void *q, void *k_cache, void *v_cache,
+                           const int32_t *block_tables, int max_blocks_per_seq,
+                           const int32_t *context_lens, float scale, void *out, int num_seqs,
+                           int num_q_heads, int num_kv_heads, int head_dim, int block_size,
+                           int64_t num_blocks, pa_layout_t layout, void *workspace,
+                           size_t workspace_bytes, void *stream) {
+    TraceRange r("pa_decode_step");
+    // every argument of both calls is checked before anything is launched
+    bool no_store = false, no_decode = false;
+    pa_status_t chk = pa::store_check_args(k, v, k_cache, v_cache, slot_mapping, num_tokens,
+                                           num_kv_heads, head_dim, block_size, num_blocks, layout,
+                                           &no_store);
+    if (chk != PA_OK) return chk;
+    chk = pa::decode_check_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, 1, scale, out, num_seqs, num_q_heads, num_kv_heads,
+                                head_dim, block_size, num_blocks, layout, 0, &no_decode);
+    if (chk != PA_OK) return chk;
+    if (!no_decode) {
+        const int gp = pa::decode_group_pad(num_q_heads / num_kv_heads);
+        const int P = plan_workers(gp, decode_kernel_choice(gp, 1), 0);
+        if (P <= 0) return PA_ERR_CUDA;
+        if (!workspace || !aligned16(workspace) ||
+            workspace_bytes < pa::decode_workspace_bytes(gp, P))
+            return PA_ERR_WORKSPACE;
+    }
+    chk = store_impl(k, v, k_cache, v_cache, slot_mapping, num_tokens, num_kv_heads, head_dim,
+                     block_size, num_blocks, layout, stream);
+    if (chk != PA_OK) return chk;
+    // with the store just queued, the decode plans its split while the store runs
+    return decode_impl(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens, 1,
+                       scale, out, num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                       num_blocks, layout, workspace, workspace_bytes, 0, stream, !no_store);
 }
 
 pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,

@@ -648,10 +648,14 @@ decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
     // L2; a prefetch reads nothing into registers, and L2 is the point of
     // coherence, so a later write by that kernel still wins. Then wait until
     // it has finished and its writes are visible before reading anything, and
-    // let the combine launch queue up behind this grid.
+    // let the combine launch queue up behind this grid. When the previous
+    // kernel is known to be this step's store (plan_early), which writes the
+    // caches only, the split of the work is planned from the lengths first.
     prefetch_inputs(a);
-    asm volatile("griddepcontrol.wait;\n" ::: "memory");
-    asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    if (!a.plan_early) {
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    }
 
     const int max_len = (int)min((int64_t)a.max_blocks_per_seq << a.block_size_log2,
                                  (int64_t)0x7fffffff);
@@ -659,6 +663,10 @@ decode_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap tmap_k,
     int p_eff;
     Cursor cc{0, 0, 0, 1, 0};
     plan_share(a, max_len, W, p_eff, T0, T1, cc);
+    if (a.plan_early) {
+        asm volatile("griddepcontrol.wait;\n" ::: "memory");
+        asm volatile("griddepcontrol.launch_dependents;\n" ::: "memory");
+    }
     const int w = blockIdx.x * kWarps + warp;
     if (w >= a.num_workers) return;
     if (T0 >= T1) {

@@ -41,7 +41,15 @@ struct DecodeArgs {
     float scale_log2;           // scale * log2(e)
     int num_workers;            // P: contiguous shares of the tile space
     int min_tiles;              // fewest tiles a share may hold (1 = exactly P shares)
+    int plan_early;             // the previous kernel writes only the caches: plan before waiting on it
 };
+
+// Host-side argument checks of the store entry points (no CUDA call); PA_OK
+// with *nothing_to_do set for an empty batch.
+pa_status_t store_check_args(const void *k, const void *v, const void *k_cache,
+                             const void *v_cache, const int64_t *slot_mapping, int64_t num_tokens,
+                             int num_kv_heads, int head_dim, int block_size, int64_t num_blocks,
+                             int layout, bool *nothing_to_do);
 
 // Host-side argument checks of every decode entry point, in the order the
 // calls apply them (pointers, sizes, layout, head_dim, block size, group

@@ -45,6 +45,8 @@ SIGNATURES = {
                           _I32, _P, _SZ, _I32, _P], _I32),
     "pa_decode_multi": ([_P, _P, _P, _P, _I32, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32, _I32,
                          _I64, _P, _SZ, _P], _I32),
+    "pa_decode_step": ([_P, _P, _P, _I64, _P, _P, _P, _P, _I32, _P, _F32, _P, _I32, _I32, _I32,
+                        _I32, _I32, _I64, _I32, _P, _SZ, _P], _I32),
     "pa_decode_multi_layout": ([_P, _P, _P, _P, _I32, _P, _I32, _F32, _P, _I32, _I32, _I32, _I32,
                                 _I32, _I64, _I32, _P, _SZ, _P], _I32),
 }
@@ -134,6 +136,52 @@ def store_kvcache(k, v, k_cache, v_cache, slot_mapping, stream=None, head_major=
                                            D, bs, NB, 1 if head_major else 0,
                                            _stream_ptr(stream, dev))
     _check("pa_store_kvcache", st)
+
+
+def decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables, context_lens,
+                scale, out=None, workspace=None, stream=None, head_major=False):
+    """One decode step through pa_decode_step: store the step's new K/V rows
+    (``k_new``, ``v_new`` bf16 [N, Hkv, D] at ``slot_mapping`` int64 [N]),
+    then single-token decode over the updated cache; returns ``out``. Same
+    results as store_kvcache followed by decode; the decode plans its work
+    split while the store runs."""
+    dev = q.device
+    for t, n, dt in ((k_new, "k_new", torch.bfloat16), (v_new, "v_new", torch.bfloat16),
+                     (slot_mapping, "slot_mapping", torch.int64), (q, "q", torch.bfloat16),
+                     (k_cache, "k_cache", torch.bfloat16), (v_cache, "v_cache", torch.bfloat16),
+                     (block_tables, "block_tables", torch.int32),
+                     (context_lens, "context_lens", torch.int32)):
+        _cuda(t, n, dt, dev)
+    S, Hq, D = q.shape
+    if head_major:
+        NB, Hkv, bs, D2 = k_cache.shape
+    else:
+        NB, bs, Hkv, D2 = k_cache.shape
+    N = slot_mapping.shape[0]
+    if v_cache.shape != k_cache.shape or D2 != D or block_tables.dim() != 2 \
+            or block_tables.shape[0] != S or context_lens.shape != (S,) \
+            or k_new.shape != (N, Hkv, D) or v_new.shape != (N, Hkv, D):
+        raise ValueError("shape mismatch between the step's tensors")
+    if out is None:
+        out = torch.empty_like(q)
+    else:
+        _cuda(out, "out", torch.bfloat16, dev)
+        if out.shape != q.shape:
+            raise ValueError("out must have q's shape")
+    if workspace is None:
+        workspace = workspace_for(Hq, Hkv, D, 0, dev)
+    else:
+        _cuda(workspace, "workspace", workspace.dtype, dev)
+    with torch.cuda.device(dev):
+        st = lib().pa_decode_step(k_new.data_ptr(), v_new.data_ptr(), slot_mapping.data_ptr(), N,
+                                  q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+                                  block_tables.data_ptr(), block_tables.shape[1],
+                                  context_lens.data_ptr(), float(scale), out.data_ptr(), S, Hq,
+                                  Hkv, D, bs, NB, 1 if head_major else 0, workspace.data_ptr(),
+                                  workspace.numel() * workspace.element_size(),
+                                  _stream_ptr(stream, dev))
+    _check("pa_decode_step", st)
+    return out
 
 
 def decode_workspace_size(num_q_heads: int, num_kv_heads: int, head_dim: int = 128,
@@ -327,8 +375,9 @@ def debug_kernel_variant(flags: int) -> None:
 
 
 class DecodeStepGraph:
-    """One decode step (store of the new K/V rows, then decode) captured into a
-    CUDA graph and replayed with one launch per step.
+    """One decode step (store of the new K/V rows, then decode, through
+    pa_decode_step) captured into a CUDA graph and replayed with one launch
+    per step.
 
     The tensors passed in are the graph's fixed buffers: update their contents
     in place (q, k_new, v_new, slot_mapping, block_tables, context_lens) and
@@ -355,9 +404,12 @@ class DecodeStepGraph:
             if host_stage is not None:
                 device_stage.copy_(host_stage, non_blocking=True)
             if has_store:
-                store_kvcache(k_new, v_new, k_cache, v_cache, slot_mapping, head_major=head_major)
-            decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=self.out,
-                   workspace=self.workspace, head_major=head_major)
+                decode_step(k_new, v_new, slot_mapping, q, k_cache, v_cache, block_tables,
+                            context_lens, scale, out=self.out, workspace=self.workspace,
+                            head_major=head_major)
+            else:
+                decode(q, k_cache, v_cache, block_tables, context_lens, scale, out=self.out,
+                       workspace=self.workspace, head_major=head_major)
             if host_out is not None:
                 host_out.copy_(self.out, non_blocking=True)
 

@@ -47,6 +47,10 @@ int main(void)
                                   int, const int32_t *, const int32_t *, int, float, void *, int,
                                   int, int, int, int, int, int64_t, pa_layout_t, void *) =
         pa_prefill_layout;
+    pa_status_t (*step)(const void *, const void *, const int64_t *, int64_t, const void *,
+                        void *, void *, const int32_t *, int, const int32_t *, float, void *, int,
+                        int, int, int, int, int64_t, pa_layout_t, void *, size_t, void *) =
+        pa_decode_step;
     pa_status_t (*take_error)(int32_t *, void *) = pa_take_device_error;
     pa_status_t (*fault_hook)(int) = pa_debug_prefill_fault;
     pa_status_t (*variant_hook)(int) = pa_debug_kernel_variant;
@@ -102,6 +106,17 @@ int main(void)
         PA_ERR_INVALID_ARG)
         ++failures;
     if (variant_hook(4) != PA_ERR_INVALID_ARG || variant_hook(0) != PA_OK)
+        ++failures;
+    /* a step with nothing to store and no sequence does nothing; a bad store
+     * argument is reported before the decode's */
+    if (step(NULL, NULL, NULL, 0, NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 0, 16, 8, 128, 16,
+             10, PA_LAYOUT_TOKEN_MAJOR, NULL, 0, NULL) != PA_OK)
+        ++failures;
+    if (step(NULL, NULL, NULL, 3, NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 2, 16, 8, 128, 16,
+             10, PA_LAYOUT_TOKEN_MAJOR, NULL, 0, NULL) != PA_ERR_INVALID_ARG)
+        ++failures;
+    if (step(NULL, NULL, NULL, 0, NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 2, 16, 8, 64, 16,
+             10, PA_LAYOUT_TOKEN_MAJOR, NULL, 0, NULL) != PA_ERR_UNSUPPORTED)
         ++failures;
     if (decode_layout(NULL, NULL, NULL, NULL, 4, NULL, 0.1f, NULL, 2, 16, 8, 128, 16, 10,
                       (pa_layout_t)3, NULL, 0, 0, NULL) != PA_ERR_INVALID_ARG)

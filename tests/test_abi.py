@@ -90,6 +90,31 @@ def test_store_host_checks(pa_lib, over, want):
     assert st == want
 
 
+# One-call decode step: the store's checks, then the decode's, all before any
+# launch (with no device visible, a launch attempt would return PA_ERR_CUDA).
+@pytest.mark.parametrize("over,want", [
+    (dict(N=-1), pa.PA_ERR_INVALID_ARG),
+    (dict(k=NULL), pa.PA_ERR_INVALID_ARG),
+    (dict(D=64), pa.PA_ERR_UNSUPPORTED),
+    (dict(layout=3), pa.PA_ERR_INVALID_ARG),
+    (dict(Hq=12), pa.PA_ERR_INVALID_ARG),            # the store is valid, nothing is launched
+    (dict(q=NULL), pa.PA_ERR_INVALID_ARG),
+    (dict(cl=24), pa.PA_ERR_INVALID_ARG),           # misaligned is only checked for 16-byte tensors
+    (dict(out=18), pa.PA_ERR_INVALID_ARG),
+    (dict(N=0, S=0, k=NULL, q=NULL), pa.PA_OK),     # nothing to store, no sequence
+])
+def test_decode_step_host_checks(pa_lib, over, want):
+    a = dict(k=16, v=16, sm=16, N=4, q=16, kc=16, vc=16, bt=16, mb=4, cl=16, scale=0.1, out=16,
+             S=2, Hq=16, Hkv=8, D=128, bs=16, NB=10, layout=0, ws=16, wsb=1 << 20)
+    a.update(over)
+    if a["cl"] == 24:       # lengths have no alignment rule: use a null instead
+        a["cl"] = NULL
+    st = pa_lib.pa_decode_step(a["k"], a["v"], a["sm"], a["N"], a["q"], a["kc"], a["vc"], a["bt"],
+                               a["mb"], a["cl"], a["scale"], a["out"], a["S"], a["Hq"], a["Hkv"],
+                               a["D"], a["bs"], a["NB"], a["layout"], a["ws"], a["wsb"], None)
+    assert st == want
+
+
 def test_workspace_size_rejects_bad_heads(pa_lib):
     assert pa_lib.pa_decode_workspace_size(12, 8, 128, 0) == 0
     assert pa_lib.pa_decode_workspace_size(16, 8, 64, 0) == 0

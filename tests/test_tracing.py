@@ -35,12 +35,14 @@ CALLS = [
      "L.pa_prefill(16, 16, 16, 16, 4, 16, 16, 8, 0.1, 16, 0, 0, 16, 8, 128, 16, 10, None)"),
     ("pa_prefill_layout",
      "L.pa_prefill_layout(16, 16, 16, 16, 4, 16, 16, 8, 0.1, 16, 0, 0, 16, 8, 128, 16, 10, 1, None)"),
+    ("pa_decode_step",
+     "L.pa_decode_step(16, 16, 16, 0, 16, 16, 16, 16, 4, 16, 0.1, 16, 0, 16, 8, 128, 16, 10, 0, 16, 1 << 20, None)"),
     ("pa_take_device_error", "L.pa_take_device_error(None, None)"),
     # an argument error: the range still closes
     ("pa_decode", "L.pa_decode(16, 16, 16, 16, 4, 16, 0.1, 16, 2, 16, 8, 64, 16, 10, 16, 1 << 20, None)"),
 ]
 
-EXPECTED_STATUS = [0] * 9 + [1, 2]     # PA_ERR_INVALID_ARG (null code), PA_ERR_UNSUPPORTED (head_dim)
+EXPECTED_STATUS = [0] * 10 + [1, 2]     # PA_ERR_INVALID_ARG (null code), PA_ERR_UNSUPPORTED (head_dim)
 
 
 def _cuda_include():
