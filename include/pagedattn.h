@@ -336,16 +336,18 @@ PA_API pa_status_t pa_prefill_layout(const void *q, const void *k_cache, const v
 
 /*
  * Device-side error record. The kernels do not fault or hang on their inputs:
- * an index outside its range is handled in a defined way, and the prefill
- * kernel's waits on the tensor cores through mbarriers are bounded (about
- * 2 s). Each such event is recorded on the device, the first code of each
- * kernel kind kept, without any synchronization in the calls themselves.
+ * an index outside its range is handled in a defined way, and every mbarrier
+ * wait is bounded (the prefill kernel's hand-offs between its warps, about
+ * 2 s; a decode warp's wait for its own tile copies, about 1 s). Each such
+ * event is recorded on the device, the first code of each kernel kind kept,
+ * without any synchronization in the calls themselves.
  * This call synchronizes `stream`, stores the smallest recorded code in *code
  * and clears every record:
  *   0  none;
  *   1  pa_prefill: shared memory not 1024-byte aligned; the launch's outputs
  *      are undefined;
- *   2  pa_prefill: a bounded wait ran out; the launch's outputs are undefined;
+ *   2  pa_prefill, or any decode call: a bounded wait ran out; the launch's
+ *      outputs are undefined;
  *   3  pa_store_kvcache: a slot outside [-1, num_blocks * block_size) was
  *      skipped; nothing is written for that row;
  *   4  pa_decode / pa_decode_multi / pa_prefill: a block-table entry that

@@ -17,7 +17,7 @@ constexpr int kTileBytes = kTileTokens * kRowBytes;  // 4 KB
 enum DeviceError : int {
     kErrNone = 0,
     kErrSmemAlign = 1,   // prefill: dynamic shared memory not 1024-byte aligned; CTA skipped
-    kErrTimeout = 2,     // prefill: a bounded mbarrier wait ran out; the launch gave up
+    kErrTimeout = 2,     // prefill or decode: a bounded mbarrier wait ran out; the launch gave up
     kErrBadSlot = 3,     // store: a slot outside [-1, num_blocks * block_size) was skipped
     kErrBadBlock = 4,    // decode / prefill: a block id outside [0, num_blocks) read as zeros
 };
