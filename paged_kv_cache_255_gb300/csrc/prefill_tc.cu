@@ -5,12 +5,19 @@
 // for prefill), computed in the flash-attention order with both contractions
 // on tcgen05.mma, S, P and O in tensor memory.
 //
-// One CTA per SM owns two 128-row query tiles A and B of one (sequence, KV
-// head); a tile is 128 / G query tokens x the G query heads of the group (G =
-// group size rounded up to a power of two), so every K/V tile fetched serves
-// 256 rows. Keys go in tiles of 128. TMEM (512 columns): S_A 0-127, O_A
-// 128-255, S_B 256-383, O_B 384-511; P_t (bf16, two per column) overwrites
-// the first 64 columns of S_t. Warp roles:
+// One CTA per SM works through items: an item is two 128-row query tiles A
+// and B of one (sequence, KV head); a tile is 128 / G query tokens x the G
+// query heads of the group (G = group size rounded up to a power of two), so
+// every K/V tile fetched serves 256 rows. Keys go in tiles of 128. TMEM (512
+// columns): S_A 0-127, O_A 128-255, S_B 256-383, O_B 384-511; P_t (bf16, two
+// per column) overwrites the first 64 columns of S_t.
+//
+// Work is handed out by grid cell (KV head, pair slot, sequence rank; heaviest
+// first in launch order). A CTA runs its own cell, then, through cluster
+// launch control, takes over cells whose CTAs have not been launched yet and
+// runs them too, keeping its TMEM, barriers and pipelines: the next item's Q
+// and first K/V tiles load while the current item finishes, and the cells are
+// still walked in launch order with a dynamic balance. Warp roles:
 //   warps 0-3, 4-7   softmax of tile A, B: thread t of the warpgroup owns row
 //                    t (TMEM lane t). Per key tile j it reads its row of S_j
 //                    (tcgen05.ld, two passes: the max, then P), masks it
@@ -24,10 +31,14 @@
 //                    landing in the 128-byte swizzled layout the MMA
 //                    descriptors name, into 3 K stages and 2 V stages. V rows
 //                    of a partly used 16-token group at the end of the keys
-//                    are copied (rows past the end zeroed) by the lanes.
-//   warp 10          Q producer: both query tiles, by TMA (a 3-D tensor map
-//                    over q: dims x heads x tokens).
-//   warp 11          issues the MMAs (converged warp, one elected lane):
+//                    are copied (rows past the end zeroed) by the lanes. The
+//                    V producer also loads each item's two query tiles by TMA
+//                    (a 3-D tensor map over q: dims x heads x tokens) once the
+//                    previous item's MMAs are done with the Q buffers (a warp
+//                    of its own for Q made the other roles' code measurably
+//                    slower). The K producer publishes the next cell once it
+//                    has issued the current one's last K tile.
+//   warp 10          issues the MMAs (converged warp, one elected lane):
 //                      S_t(j)  = Q_t K_j^T      M 128, N 128, K 16 x 8 (smem, smem)
 //                      O_t    += P_t(j) V_j     M 128, N 128, K 16 x 8 (TMEM, smem)
 //                    as soon as their inputs are ready; S_t(j + 1) follows
@@ -39,8 +50,9 @@
 //
 // Hand-offs are mbarriers: k_full / v_full complete when the TMA bytes have
 // landed and the producer warp has arrived (after fencing its own
-// shared-memory writes to the async proxy); q_full when the Q warp's copies
-// have landed and been fenced; tcgen05.commit arrives on s_full, pv_done,
+// shared-memory writes to the async proxy); q_full when the Q copies have
+// landed; unit_full / unit_empty hand the next cell's descriptor from the K
+// producer to the other warps; tcgen05.commit arrives on s_full, pv_done,
 // k_empty and v_empty; the softmax warps arrive on p_ready once P is in TMEM
 // (and O rescaled), and on o_free once the epilogue has read O. Every wait is
 // bounded (about 2 s) and also gives up once any thread of the CTA has
@@ -71,9 +83,8 @@ constexpr int kVStages = 2;
 constexpr int kSoftmaxThreads = 256;
 constexpr int kKWarp = kSoftmaxThreads / 32;             // 8
 constexpr int kVWarp = kKWarp + 1;                       // 9
-constexpr int kQWarp = kKWarp + 2;                       // 10
-constexpr int kMmaWarp = kKWarp + 3;                     // 11
-constexpr int kThreads = kSoftmaxThreads + 4 * 32;
+constexpr int kMmaWarp = kKWarp + 2;                     // 10
+constexpr int kThreads = kSoftmaxThreads + 3 * 32;
 constexpr int kGroup = 16;                               // tokens per TMA box
 constexpr int kGroups = kKeys / kGroup;                  // 8
 constexpr uint32_t kQBytes = kRows * kRowBytes;         // 32 KB: 2 K-halves of [128][128 B]
@@ -95,18 +106,24 @@ constexpr uint32_t kBarSFull = kBarVEmpty + kVStages;    // + query tile (A 0, B
 constexpr uint32_t kBarPReady = kBarSFull + 2;
 constexpr uint32_t kBarPVDone = kBarPReady + 2;
 constexpr uint32_t kBarOFree = kBarPVDone + 2;
-constexpr uint32_t kNumBars = kBarOFree + 2;
+constexpr uint32_t kBarUnitFull = kBarOFree + 2;         // + unit ring slot
+constexpr uint32_t kBarUnitEmpty = kBarUnitFull + 2;     // + unit ring slot
+constexpr uint32_t kBarClc = kBarUnitEmpty + 2;          // launch-control responses
+constexpr uint32_t kNumBars = kBarClc + 1;
 constexpr uint32_t kOffTmemSlot = kOffCtl + 8 * kNumBars;
 constexpr uint32_t kOffAbort = kOffTmemSlot + 4;
-constexpr uint32_t kOffSeqSlot = kOffAbort + 4;
-// heavy-first sequence order (up to kRankMaxSeqs sequences): their lengths and
-// query starts, staged once per CTA
+// heavy-first sequence order (up to kRankMaxSeqs sequences): their lengths,
+// query starts and the sequence of each rank, staged once per CTA
 constexpr int kRankMaxSeqs = 256;
 constexpr uint32_t kOffSeqLens = kOffCtl + 256;
 constexpr uint32_t kOffSeqStarts = kOffSeqLens + 4 * kRankMaxSeqs;
-constexpr uint32_t kSmemBytes = kOffSeqStarts + 4 * (kRankMaxSeqs + 1) + 12;
-static_assert(kOffSeqSlot + 4 <= kOffSeqLens, "control block");
+constexpr uint32_t kOffRankSeq = kOffSeqStarts + 4 * (kRankMaxSeqs + 1);       // uint16 per rank
+constexpr uint32_t kOffUnits = (kOffRankSeq + 2 * kRankMaxSeqs + 15) & ~15u;  // 2 UnitDesc
+constexpr uint32_t kOffClcResp = kOffUnits + 64;                              // 16 B, 16-aligned
+constexpr uint32_t kSmemBytes = kOffClcResp + 16;
+static_assert(kOffAbort + 4 <= kOffSeqLens, "control block");
 static_assert(kSmemBytes <= 232448, "shared memory");
+constexpr int kUnitReaders = kThreads / 32;              // every warp reads each unit
 constexpr uint32_t kTmemCols = 512;
 constexpr uint32_t kIdescS = tc::idesc_bf16(128, kKeys, false);
 constexpr uint32_t kIdescPV = tc::idesc_bf16(128, 128, true);
@@ -225,6 +242,19 @@ __device__ __forceinline__ int groups_full(int k0, int kend) {
     return n < 0 ? 0 : (n > kGroups ? kGroups : n);
 }
 
+// A unit of work is one grid cell: KV head x, pair slot y of the sequence of
+// rank z. A CTA starts with its own cell and then takes over cells whose CTAs
+// have not been launched yet (cluster launch control), so the persistent CTAs
+// walk the grid in its launch order. The descriptors of the current and the
+// next unit sit in a two-entry ring in shared memory.
+struct UnitDesc {
+    int valid;      // 0: no unit (the end of this CTA's walk)
+    int kvh, y, s;  // KV head, pair slot, sequence
+    int q0, n, L;   // first query row, query rows, context length
+    int np;         // query-tile pairs of the sequence's chunk
+};
+static_assert(sizeof(UnitDesc) == 32, "unit descriptor");
+
 // Work item: a pair of query tiles (2 x 128 / G tokens) of one (sequence, KV
 // head). Every role walks the same items and computes the same bounds.
 struct Item {
@@ -263,6 +293,72 @@ __device__ __forceinline__ Item make_item(int qp, int n, int L) {
     return it;
 }
 
+// The unit of grid cell (x, y, z), from the staged sequence tables (or from
+// global memory beyond kRankMaxSeqs sequences, where z is the sequence).
+template <int G>
+__device__ __forceinline__ UnitDesc decode_unit(const PrefillArgs &a, const uint8_t *smem, int x,
+                                                int y, int z, int64_t max_len) {
+    constexpr int BT = kRows / G;
+    UnitDesc u;
+    int q0, q1, L;
+    if (a.num_seqs <= kRankMaxSeqs) {
+        const int *lens = reinterpret_cast<const int *>(smem + kOffSeqLens);
+        const int *starts = reinterpret_cast<const int *>(smem + kOffSeqStarts);
+        const uint16_t *rank_seq = reinterpret_cast<const uint16_t *>(smem + kOffRankSeq);
+        u.s = rank_seq[z];
+        q0 = starts[u.s];
+        q1 = starts[u.s + 1];
+        L = lens[u.s];
+    } else {
+        u.s = z;
+        q0 = __ldg(a.query_start_loc + z);
+        q1 = __ldg(a.query_start_loc + z + 1);
+        const int64_t l = __ldg(a.context_lens + z);
+        L = (int)(l < 0 ? 0 : (l > max_len ? max_len : l));
+    }
+    q0 = q0 < 0 ? 0 : (q0 > a.total_q ? a.total_q : q0);
+    q1 = q1 < q0 ? q0 : (q1 > a.total_q ? a.total_q : q1);
+    u.kvh = x;
+    u.y = y;
+    u.q0 = q0;
+    u.n = q1 - q0;
+    u.L = L;
+    u.np = (u.n + 2 * BT - 1) / (2 * BT);
+    u.valid = pair_of(0, y, gridDim.y, u.np) >= 0 ? 1 : 0;
+    return u;
+}
+
+// Cluster launch control: ask to take over a CTA of this grid that has not
+// been launched yet. The 16-byte response lands at `resp` and completes a
+// phase of `bar` (the caller has armed it for 16 bytes).
+__device__ __forceinline__ void clc_try_cancel(uint32_t resp, uint32_t bar) {
+    asm volatile(
+        "clusterlaunchcontrol.try_cancel.async.shared::cta.mbarrier::complete_tx::bytes.b128 "
+        "[%0], [%1];\n" ::"r"(resp),
+        "r"(bar)
+        : "memory");
+}
+// Decode a response: true and the taken CTA's index when a CTA was taken.
+__device__ __forceinline__ bool clc_taken(uint32_t resp, int &x, int &y, int &z) {
+    uint32_t ok, cx = 0, cy = 0, cz = 0;
+    asm volatile(
+        "{\n .reg .b128 h;\n .reg .pred p;\n ld.shared.b128 h, [%4];\n"
+        " clusterlaunchcontrol.query_cancel.is_canceled.pred.b128 p, h;\n"
+        " selp.u32 %0, 1, 0, p;\n"
+        " @p clusterlaunchcontrol.query_cancel.get_first_ctaid.v4.b32.b128 {%1, %2, %3, _}, h;\n}\n"
+        : "=r"(ok), "+r"(cx), "+r"(cy), "+r"(cz)
+        : "r"(resp)
+        : "memory");
+    x = (int)cx;
+    y = (int)cy;
+    z = (int)cz;
+    return ok != 0;
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;\n" ::"r"(bar), "r"(bytes)
+                 : "memory");
+}
+
 template <int G>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_k,
@@ -271,22 +367,21 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
     constexpr int BT = kRows / G;               // query tokens per query tile
     extern __shared__ __align__(1024) uint8_t smem[];
     const int tid = threadIdx.x, warp = tid >> 5;
-    const int kvh = blockIdx.x;
     const int g = a.group;
     const int64_t max_len = (int64_t)a.max_blocks_per_seq << a.block_size_log2;
 
-    // Grid (KV head x, pair slot y, sequence z). The block scheduler starts
-    // CTAs in grid order (x fastest, z slowest), so with few enough sequences
-    // slice z takes the one of rank z by context length (longest first, ties
-    // by index), every KV head of its heaviest pair first: the longest work
-    // of the whole launch starts first and the last wave holds the shortest.
-    // Every CTA ranks the same staged lengths, so the slices map one to one
-    // onto the sequences.
-    int s = blockIdx.z, q0, q1, L;
+    // Grid (KV head x, pair slot y, sequence rank z). The block scheduler
+    // starts CTAs in grid order (x fastest, z slowest), so with few enough
+    // sequences slice z takes the one of rank z by context length (longest
+    // first, ties by index), every KV head of its heaviest pair first: the
+    // longest work of the whole launch starts first and the last wave holds
+    // the shortest. Every CTA ranks the same staged lengths. A CTA that runs
+    // out of work takes over the next CTA not launched yet, so the grid order
+    // is also the order in which the persistent CTAs walk the cells.
     if (a.num_seqs <= kRankMaxSeqs) {
         int *lens = reinterpret_cast<int *>(smem + kOffSeqLens);
         int *starts = reinterpret_cast<int *>(smem + kOffSeqStarts);
-        volatile int *slot = reinterpret_cast<volatile int *>(smem + kOffSeqSlot);
+        uint16_t *rank_seq = reinterpret_cast<uint16_t *>(smem + kOffRankSeq);
         if (tid < a.num_seqs) {
             const int64_t l = __ldg(a.context_lens + tid);
             lens[tid] = (int)(l < 0 ? 0 : (l > max_len ? max_len : l));
@@ -300,24 +395,16 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 const int li = lens[i];
                 rank += (li > lj || (li == lj && i < tid)) ? 1 : 0;
             }
-            if (rank == (int)blockIdx.z) *slot = tid;
+            rank_seq[rank] = (uint16_t)tid;
         }
         __syncthreads();
-        s = *slot;
-        q0 = starts[s];
-        q1 = starts[s + 1];
-        L = lens[s];
-    } else {
-        q0 = __ldg(a.query_start_loc + s);
-        q1 = __ldg(a.query_start_loc + s + 1);
-        const int64_t l = __ldg(a.context_lens + s);
-        L = (int)(l < 0 ? 0 : (l > max_len ? max_len : l));
     }
-    q0 = q0 < 0 ? 0 : (q0 > a.total_q ? a.total_q : q0);
-    q1 = q1 < q0 ? q0 : (q1 > a.total_q ? a.total_q : q1);
-    const int n = q1 - q0;
-    const int np = (n + 2 * BT - 1) / (2 * BT);            // query-tile pairs of the chunk
-    if (pair_of(0, blockIdx.y, gridDim.y, np) < 0) return;
+    UnitDesc *units = reinterpret_cast<UnitDesc *>(smem + kOffUnits);
+    {
+        const UnitDesc u0 = decode_unit<G>(a, smem, blockIdx.x, blockIdx.y, blockIdx.z, max_len);
+        if (!u0.valid) return;                  // this cell holds no pair
+        if (tid == 0) units[0] = u0;
+    }
 
     const uint32_t sbase = smem_u32(smem);
     if (sbase & 1023u) {                        // the swizzle atoms need 1024-byte alignment
@@ -344,9 +431,13 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             tc::mbar_init(bar(kBarPReady + i), kRows / 32);
             tc::mbar_init(bar(kBarPVDone + i), 1);
             tc::mbar_init(bar(kBarOFree + i), kRows / 32);
+            tc::mbar_init(bar(kBarUnitFull + i), 1);
+            tc::mbar_init(bar(kBarUnitEmpty + i), kUnitReaders);
         }
+        tc::mbar_init(bar(kBarClc), 1);
         *abort = 0;
         tc::fence_mbar_init();
+        mbar_arrive(bar(kBarUnitFull));         // unit 0 (this CTA's own cell) is published
     }
     if (warp == kMmaWarp) tc::tmem_alloc(sbase + kOffTmemSlot, kTmemCols);
     tc::fence_before_sync();
@@ -366,8 +457,16 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         uint32_t gt = 0;                        // this query tile's key tiles before this item
         bool ok = true;
 #pragma unroll 1
+        for (int k = 0; ok; ++k) {
+        // unit k of this CTA's walk; its fields are read from shared memory
+        // where they are used, so none stays live across the tile loop
+        const volatile UnitDesc &u = units[k & 1];
+        if (!warp_wait(bar(kBarUnitFull + (k & 1)), (k >> 1) & 1, abort)) { ok = false; break; }
+        if (!u.valid) break;
+#pragma unroll 1
         for (int i = 0; ok; ++i) {
-            const int qp = pair_of(i, blockIdx.y, gridDim.y, np);
+            const int n = u.n, L = u.L;
+            const int qp = pair_of(i, u.y, gridDim.y, u.np);
             if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             const int tok = it.tok0 + wg * BT + r / G, head = r % G;
@@ -483,7 +582,7 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 tc::fence_after_sync();
             }
             const float inv = lsum > 0.f ? 1.f / lsum : 0.f;
-            const int64_t row_elem = ((int64_t)q0 + tok) * a.num_q_heads + (int64_t)kvh * g + head;
+            const int64_t row_elem = ((int64_t)u.q0 + tok) * a.num_q_heads + (int64_t)u.kvh * g + head;
             uint4 *orow = reinterpret_cast<uint4 *>(static_cast<char *>(a.out) + row_elem * kRowBytes);
 #pragma unroll 1
             for (int ch = 0; ch < 4; ++ch) {
@@ -511,6 +610,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             warp_arrive(bar(kBarOFree + wg));
             gt += ntt;
         }
+        if (ok) warp_arrive(bar(kBarUnitEmpty + (k & 1)));
+        }
     } else if (warp == kKWarp || warp == kVWarp) {
         // ---------------- K and V producers ----------------
         // Per key tile, lane i < 16 loads the box of 16-key group i / 2, half
@@ -527,13 +628,36 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         const uint32_t bar_empty = bar(is_v ? kBarVEmpty : kBarKEmpty);
         const uint32_t base = sbase + (is_v ? kOffV : kOffK);
         uint32_t gt = 0;
+        uint32_t clc_n = 0;                     // launch-control requests made (K warp)
+        int qitem = 0;                          // items whose Q the V warp has loaded
+        bool clc_done = false;                  // a request found no CTA left to take
         bool ok = true;
 #pragma unroll 1
+        for (int k = 0; ok; ++k) {
+        if (!warp_wait(bar(kBarUnitFull + (k & 1)), (k >> 1) & 1, abort)) { ok = false; break; }
+        const UnitDesc u = units[k & 1];
+        if (!u.valid) break;
+        const int s = u.s, kvh = u.kvh, n = u.n, L = u.L, q0 = u.q0;
+#pragma unroll 1
         for (int i = 0; ok; ++i) {
-            const int qp = pair_of(i, blockIdx.y, gridDim.y, np);
+            const int qp = pair_of(i, u.y, gridDim.y, u.np);
             if (qp < 0) break;
             const Item it = make_item<G>(qp, n, L);
             const int kend = it.kend;
+            if (is_v) {
+                // the V producer also loads each item's Q tiles, once the
+                // previous item's MMAs are done with the Q buffers
+                if (qitem > 0 && !warp_wait(bar(kBarQEmpty), (qitem - 1) & 1, abort)) { ok = false; break; }
+                if (lane == 0) {
+                    tc::mbar_expect_tx(bar(kBarQFull), 2 * kQBytes);
+                    for (int t = 0; t < 2; ++t)
+                        for (int hh = 0; hh < 2; ++hh)
+                            tc::tma_load_3d(sbase + kOffQ + t * kQBytes + hh * kQHalf, &tmap_q, hh * 64,
+                                            kvh * g, q0 + it.tok0 + t * BT, bar(kBarQFull));
+                }
+                warp_arrive(bar(kBarQFull));
+                ++qitem;
+            }
             // TMA coordinates (dim 1, dim 2) of this lane's box of tile j:
             // token-major (KV head, slot), head-major (offset in the block,
             // block * Hkv + KV head); dim 1 at -kGroup reads zeros (a bad block
@@ -574,32 +698,43 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             }
             gt += it.nt;
         }
-    } else if (warp == kQWarp) {
-        // ---------------- Q producer ----------------
-        const int lane = tid & 31;
-        int item = 0;
-        bool ok = true;
-#pragma unroll 1
-        for (int i = 0; ok; ++i, ++item) {
-            const int qp = pair_of(i, blockIdx.y, gridDim.y, np);
-            if (qp < 0) break;
-            const Item it = make_item<G>(qp, n, L);
-            if (item > 0 && !warp_wait(bar(kBarQEmpty), (item - 1) & 1, abort)) { ok = false; break; }
-            // Q_A and Q_B: row r of tile t is token tok0 + t BT + r / G, head
-            // kvh g + r % G. One TMA box of 64 dims x G heads x BT tokens per
-            // tile half lands as those 128 rows of 128 B, 128-byte swizzled, as
-            // the S descriptors read them. Rows past the chunk or the group's
-            // heads hold other rows' values, or zeros past the tensor: each row
-            // of S, P and O depends on its own q row only, and those rows are
-            // never written out.
+        if (!ok) break;
+        warp_arrive(bar(kBarUnitEmpty + (k & 1)));
+        if (is_v) continue;
+        // The K warp publishes unit k + 1 once it has issued unit k's last K
+        // tile: it takes over the next CTA of the grid not launched yet
+        // (cells with no pair are taken and skipped). Once a request finds no
+        // CTA left, no further request is made and the published unit marks
+        // the end of the walk.
+        UnitDesc nx{};
+        nx.valid = 0;
+        while (!clc_done) {
+            // every lane has read the previous response; the next one is
+            // written through the async proxy
+            __syncwarp();
+            tc::fence_proxy_async();
             if (lane == 0) {
-                tc::mbar_expect_tx(bar(kBarQFull), 2 * kQBytes);
-                for (int t = 0; t < 2; ++t)
-                    for (int h = 0; h < 2; ++h)
-                        tc::tma_load_3d(sbase + kOffQ + t * kQBytes + h * kQHalf, &tmap_q, h * 64,
-                                        kvh * g, q0 + it.tok0 + t * BT, bar(kBarQFull));
+                mbar_arrive_expect_tx(bar(kBarClc), 16);
+                clc_try_cancel(sbase + kOffClcResp, bar(kBarClc));
             }
-            warp_arrive(bar(kBarQFull));
+            if (!warp_wait(bar(kBarClc), clc_n & 1, abort)) { ok = false; break; }
+            ++clc_n;
+            int cx, cy, cz;
+            if (!clc_taken(sbase + kOffClcResp, cx, cy, cz)) {
+                clc_done = true;
+                break;
+            }
+            nx = decode_unit<G>(a, smem, cx, cy, cz, max_len);
+            if (nx.valid) break;
+        }
+        if (!ok) break;
+        // its ring slot held unit k - 1, which every warp has finished
+        if (k >= 1 && !warp_wait(bar(kBarUnitEmpty + ((k + 1) & 1)), ((k - 1) >> 1) & 1, abort)) {
+            ok = false;
+            break;
+        }
+        if (lane == 0) units[(k + 1) & 1] = nx;
+        warp_arrive(bar(kBarUnitFull + ((k + 1) & 1)));
         }
     } else if (warp == kMmaWarp) {
         // ---------------- MMA issue ----------------
@@ -670,10 +805,15 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         int item = 0;
         bool ok = true;
 #pragma unroll 1
+        for (int k = 0; ok; ++k) {
+        if (!warp_wait(bar(kBarUnitFull + (k & 1)), (k >> 1) & 1, abort)) { ok = false; break; }
+        const volatile UnitDesc &u = units[k & 1];
+        if (!u.valid) break;
+#pragma unroll 1
         for (int i = 0; ok; ++i, ++item) {
-            const int qp = pair_of(i, blockIdx.y, gridDim.y, np);
+            const int qp = pair_of(i, u.y, gridDim.y, u.np);
             if (qp < 0) break;
-            const Item it = make_item<G>(qp, n, L);
+            const Item it = make_item<G>(qp, u.n, u.L);
             ok = warp_wait(bar(kBarQFull), item & 1, abort);
             int sj0 = 0, sj1 = 0, pj0 = 0, pj1 = 0;     // next S / PV tile of A, B
             uint64_t t_idle = 0;
@@ -741,6 +881,8 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
             gt += it.nt;
             gq0 += it.nta;
             gq1 += it.ntb;
+        }
+        if (ok) warp_arrive(bar(kBarUnitEmpty + (k & 1)));
         }
     }
 
