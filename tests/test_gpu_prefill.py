@@ -201,6 +201,35 @@ def test_full_size_sampled_rows(name):
     assert torch.isfinite(out.float()).all()
 
 
+def test_launches_on_two_streams_at_once():
+    """Persistent CTAs take over only CTAs of their own grid: two prefill
+    launches running at the same time on two streams, each grid several times
+    the SM count, both match the oracle. The batches differ in group size and
+    length mix, so a cell handed across grids would be detected."""
+    specs = [(_spec("two_a", 32, 8, 16), [3000, 900, 2200, 64, 1500, 4000], [600, 900, 128, 64, 1, 700]),
+             (_spec("two_b", 16, 8, 32), [700, 1800, 300, 2500, 90], [700, 400, 300, 513, 90])]
+    jobs = []
+    for i, (spec, lens, chunks) in enumerate(specs):
+        pb = inputs.prefill_batch(spec, seed=90 + i, context_lens=lens, chunk_lens=chunks)
+        kc, vc = _oracle_caches(pb)
+        ref = oracle.get().prefill(pb.q, kc, vc, pb.wl.block_tables, pb.wl.context_lens,
+                                   pb.query_start_loc, pb.wl.scale)
+        d = _device(pb)
+        if pb.slot_mapping.shape[0]:
+            pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+        jobs.append((pb, d, ref))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream() for _ in jobs]
+    outs = []
+    for (pb, d, _), st in zip(jobs, streams):
+        with torch.cuda.stream(st):
+            outs.append(pa.prefill(d["q"], d["k_cache"], d["v_cache"], d["block_tables"],
+                                   d["context_lens"], d["qsl"], pb.wl.scale))
+    torch.cuda.synchronize()
+    for (pb, _, ref), out in zip(jobs, outs):
+        gu.assert_close(out, ref, pb.wl.spec.name)
+
+
 def test_rejects_bad_shapes():
     spec = _spec("j", 16, 8, 16)
     pb = inputs.prefill_batch(spec, seed=65, context_lens=[20], chunk_lens=[20])
