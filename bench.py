@@ -41,8 +41,18 @@ from paged_kv_cache_255_gb300 import inputs  # noqa: E402
 
 METRIC = "paged-decode µs/step and KV-read GB/s (fraction of GB300 HBM peak)"
 DEFAULT_WORKLOAD = "long_context"
-# decode and prefill steps measured beside the headline (sub-records)
-SUB_DECODE = ["large_batch", "qwen3_0_6b", "prefix_shared", "tiny"]
+# decode and prefill steps measured beside the headline (sub-records): name ->
+# (workload, query tokens per sequence, pool layout)
+SUB_DECODE = {
+    "large_batch": ("large_batch", 1, "token_major"),
+    "qwen3_0_6b": ("qwen3_0_6b", 1, "token_major"),
+    "prefix_shared": ("prefix_shared", 1, "token_major"),
+    "tiny": ("tiny", 1, "token_major"),
+    # multi-token decode: 4 new tokens per sequence (speculative verification)
+    "qwen3_0_6b_q4": ("qwen3_0_6b", 4, "token_major"),
+    # the headline step on a head-major pool [NB, Hkv, bs, D]
+    "long_context_head_major": ("long_context", 1, "head_major"),
+}
 SUB_PREFILL = ["chunked_8b", "qwen3_0_6b_prompts"]
 L2_FLUSH_BYTES = 512 << 20       # > 2x the 129 MB L2
 L2_NOTE = "flushed between steps (512 MiB write)"
@@ -459,10 +469,11 @@ def decode_rates(st: DecodeStep, t):
 
 
 def decode_sub_record(name, args, dev, flush, stream, world):
-    wl = inputs.generate(workload_spec(args, name), seed=0, device=dev)
-    st = DecodeStep(wl, dev)
+    workload, q_len, layout = SUB_DECODE[name]
+    wl = inputs.generate(workload_spec(args, workload), seed=0, device=dev)
+    st = DecodeStep(wl, dev, layout, q_len)
     t = time_decode(st, flush, stream, args.steps, args.warmup, world)
-    rec = {"config": workload_config(wl), **decode_rates(st, t),
+    rec = {"config": workload_config(wl, q_len, layout), **decode_rates(st, t),
            "gpu_launches": args.steps * st.launches_per_step()}
     del st, wl
     torch.cuda.empty_cache()
@@ -592,8 +603,8 @@ def run_gpu(args, rank, world, local):
     # ---- the other decode steps and the prefill steps, timed the same way
     subs = {}
     if not args.no_sub_records:
-        for name in SUB_DECODE:
-            if name != args.workload:
+        for name, (workload, q_len, layout) in SUB_DECODE.items():
+            if (workload, q_len, layout) != (args.workload, args.q_len, args.layout):
                 subs[name] = decode_sub_record(name, args, dev, flush, stream, world)
         for name in SUB_PREFILL:
             subs[name] = prefill_sub_record(name, args, dev, flush, stream, world)
