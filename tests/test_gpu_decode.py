@@ -161,3 +161,48 @@ def test_full_size_sampled(name):
     # any size: finite, and a convex combination of N(0,1) rows stays small
     assert torch.isfinite(out).all()
     assert out.float().abs().max().item() < 6.0
+
+
+def test_full_size_step_on_head_major_pool():
+    """The headline step on a head-major pool, as the benchmark runs it: one
+    pa_decode_step call; every head of the 8 longest sequences and 40 more
+    sampled outputs against the oracle, the pool bit-exact after the store."""
+    wl = inputs.generate(SP["long_context"], seed=0, device="cuda")
+    host_k, host_v = wl.k_cache.cpu(), wl.v_cache.cpu()
+    kc = wl.k_cache.permute(0, 2, 1, 3).contiguous()
+    vc = wl.v_cache.permute(0, 2, 1, 3).contiguous()
+    del wl.k_cache, wl.v_cache
+    out = pa.decode_step(wl.k_new, wl.v_new, torch.from_numpy(wl.slot_mapping).cuda(), wl.q, kc,
+                         vc, torch.from_numpy(wl.block_tables).cuda(),
+                         torch.from_numpy(wl.context_lens).cuda(), wl.scale, head_major=True)
+    torch.cuda.synchronize()
+    assert pa.take_device_error() == 0
+    O = oracle.get()
+    rk, rv = O.store_kvcache(wl.k_new.cpu(), wl.v_new.cpu(), host_k, host_v, wl.slot_mapping)
+    got_k = gu.host_bits(kc.permute(0, 2, 1, 3).contiguous())
+    assert np.array_equal(got_k, rk)
+    pairs = _sample_pairs(wl, 40, seed=2)
+    ref = O.decode_pairs(wl.q.cpu(), rk, rv, wl.block_tables, wl.context_lens, wl.scale, pairs)
+    got = out[torch.from_numpy(pairs[:, 0]).long(), torch.from_numpy(pairs[:, 1]).long()]
+    gu.assert_close(got, ref, "long_context head-major")
+
+
+def test_full_size_multi_token_decode():
+    """The qwen3-shaped step with 4 new query tokens per sequence, as the
+    benchmark runs it (the step's store, then pa_decode_multi): every output
+    against the oracle."""
+    wl = inputs.generate(SP["qwen3_0_6b"], seed=0, device="cuda")
+    host_k, host_v = wl.k_cache.cpu(), wl.v_cache.cpu()
+    g = torch.Generator().manual_seed(11)
+    S, Hq, D = wl.q.shape
+    q = torch.randn((S, 4, Hq, D), generator=g).to(torch.bfloat16)
+    d = gu.device_inputs(wl)
+    pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+    out = pa.decode_multi(q.cuda(), d["k_cache"], d["v_cache"], d["block_tables"],
+                          d["context_lens"], wl.scale)
+    torch.cuda.synchronize()
+    assert pa.take_device_error() == 0
+    O = oracle.get()
+    rk, rv = O.store_kvcache(wl.k_new.cpu(), wl.v_new.cpu(), host_k, host_v, wl.slot_mapping)
+    ref = O.decode_multi(q, rk, rv, wl.block_tables, wl.context_lens, wl.scale)
+    gu.assert_close(out, ref, "qwen3 Q=4")
