@@ -33,7 +33,9 @@
  * Ownership: every pointer is caller-owned memory on the current CUDA device
  * (the workspace included). The library allocates nothing and keeps no data
  * between calls; its only process-wide state is the NVTX domain handle (see
- * Tracing) and the static scratch of pa_decode_noalloc. Calls are
+ * Tracing), the static scratch of pa_decode_noalloc, the test hooks, and per
+ * device the SM count and the decode's worker counts, computed on the first
+ * call on that device. Calls are
  * asynchronous on `stream` (a cudaStream_t; NULL is the legacy default
  * stream) and return once the kernels are queued.
  *

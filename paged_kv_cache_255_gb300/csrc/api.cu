@@ -45,10 +45,28 @@ int log2_exact(int x) {
 
 bool block_size_ok(int bs) { return bs >= 16 && bs <= 256 && log2_exact(bs) >= 0; }
 
+// Per-device values the calls need on every launch, computed on a device's
+// first call and kept: its SM count, and the decode's worker count for each
+// padded group size (1, 2, 4, 8, 16) and tile kind (both depend only on the
+// device and the kernels' resources). A racing first call computes the same
+// value twice.
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+std::atomic<int> g_workers[kMaxDevices][5][2];
+
+int current_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return -1;
+    return dev;
+}
+
 int current_sm_count() {
-    int dev = 0, n = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    int n = g_sm_count[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
     if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+    g_sm_count[dev].store(n, std::memory_order_relaxed);
     return n;
 }
 
@@ -69,8 +87,17 @@ pa::DecodeKernel decode_kernel_choice(int group_pad, int q_len) {
 // Shares of the tile space for a call: forced, or from the device.
 int plan_workers(int group_pad, pa::DecodeKernel k, int num_partitions) {
     if (num_partitions > 0) return num_partitions;
+    const int dev = current_device();
+    if (dev < 0) return 0;
+    int gi = 0;
+    while ((1 << gi) < group_pad && gi < 4) ++gi;
+    std::atomic<int> &slot = g_workers[dev][gi][k == pa::DecodeKernel::kSimt ? 1 : 0];
+    int P = slot.load(std::memory_order_relaxed);
+    if (P > 0) return P;
     const int sms = current_sm_count();
-    return sms > 0 ? pa::decode_default_workers(group_pad, k, sms) : 0;
+    P = sms > 0 ? pa::decode_default_workers(group_pad, k, sms) : 0;
+    if (P > 0) slot.store(P, std::memory_order_relaxed);
+    return P;
 }
 
 pa_status_t decode_impl(const void *q, const void *k_cache, const void *v_cache,
