@@ -67,10 +67,16 @@ FULL_STEP_LIMIT_S = 30.0
 
 
 def kernel_hash() -> str:
+    """Hash of the decode kernel's code (comments and whitespace removed, so
+    that an edited comment does not invalidate counters taken on the same
+    code)."""
     h = hashlib.sha256()
     for p in KERNEL_SOURCES:
-        with open(os.path.join(ROOT, p), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, p)) as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

@@ -14,7 +14,9 @@
 //     flat tile space of W tiles.
 //   * P workers (one warp each, persistent: P = SMs x resident CTAs x warps)
 //     take equal contiguous shares [w W / P, (w + 1) W / P) of that space, so
-//     every SM streams the same number of bytes whatever the length mix.
+//     every SM streams the same number of bytes whatever the length mix. Every
+//     CTA plans the split from context_lens in its prologue (before waiting on
+//     the previous kernel when that is the same step's store).
 //   * A worker streams its tiles through a private kStages-deep ring in shared
 //     memory. One lane fills a stage with four TMA boxes (the K tile and the
 //     V tile, each 16 rows x 64 head dims twice, 128-byte swizzle) counted
@@ -28,7 +30,9 @@
 //   * MmaTile: q.K^T and P.V on the tensor cores with mma.sync m16n8k16 bf16
 //     (fp32 accumulate): 16 tokens x 8 (or 16) query heads x 128 dims per
 //     tile; the default.
-//   * SimtTile: the same on the CUDA cores, lane l owning dims [4l, 4l + 4).
+//   * SimtTile: the same on the CUDA cores, lane l owning dims [4l, 4l + 4);
+//     kept as the comparison and a second parity path, selected only by the
+//     test hook pa_debug_kernel_variant.
 // The kernels never wait on one another inside a launch; a warp waits only on
 // its own copies, and every such wait is bounded (1 s, then the launch records
 // code 2 and the warp exits).
