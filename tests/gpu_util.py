@@ -51,6 +51,9 @@ def gpu_step(wl, num_partitions=0, d=None):
     out = pa.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
                     wl.scale, num_partitions=num_partitions)
     torch.cuda.synchronize()
+    # nothing may have been skipped, zero-filled or timed out on the way
+    code = pa.take_device_error()
+    assert code == 0, f"the store or decode recorded device error {code}"
     return out, d["k_cache"], d["v_cache"]
 
 
