@@ -4,16 +4,19 @@ then decode attention) on synthetic inputs, timed with CUDA events.
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl reference]
 
 Prints one JSON line (rank 0). ``value`` is microseconds per step (store +
-decode, inputs resident in HBM, L2 flushed between steps) on the headline
-workload: the skewed long-context decode step (8 sequences of 32k-131k tokens
-among 120 short ones, 32 q / 8 KV heads), the largest of the decode steps.
+decode, inputs resident in HBM) on the headline workload: the skewed
+long-context decode step (8 sequences of 32k-131k tokens among 120 short
+ones, 32 q / 8 KV heads), the largest of the decode steps. Its 2.3 GB of K/V
+reads are 18x the L2, so its steps run back to back (inputs larger than L2);
+steps that read less than 8x the L2 are preceded by an L2 flush (a 512 MiB
+write), and ``l2_alt`` gives each large step flushed as well.
 ``roofline`` reports the decode launch's KV-read bandwidth against the
 measured HBM copy peak; ``e2e`` repeats the step through host buffers (pinned
 H2D of the step's inputs and D2H of its output inside the timed region);
 ``cpu_baseline`` times the fp64 CPU oracle on the whole step, on one thread
 and on all host cores. ``workloads`` holds the other decode steps and the two
-prefill steps, each timed the same way (store + call, L2 flushed between
-steps) with its own roofline fraction. ``--impl reference`` times only the
+prefill steps, each timed the same way (store + call; the prefill steps
+always with the L2 flushed) with its own roofline fraction. ``--impl reference`` times only the
 oracle (the reference arm). With N > 1 (torchrun) every rank runs its own
 replica of the step on its own GPU: the path has no cross-GPU exchange.
 """
@@ -54,8 +57,19 @@ SUB_DECODE = {
     "long_context_head_major": ("long_context", 1, "head_major"),
 }
 SUB_PREFILL = ["chunked_8b", "qwen3_0_6b_prompts"]
-L2_FLUSH_BYTES = 512 << 20       # > 2x the 129 MB L2
-L2_NOTE = "flushed between steps (512 MiB write)"
+L2_BYTES = 129_000_000           # GB300 L2
+L2_FLUSH_BYTES = 512 << 20       # > 2x the L2
+# A decode step whose K/V reads are at least this many times the L2 runs its
+# timed steps back to back (inputs larger than L2: each step streams them
+# through L2 many times over, so nothing of one step is left for the next);
+# smaller steps get the L2 flush before each step. The flush is a write, and
+# the lines it leaves dirty are written back to HBM during the next step.
+LARGE_INPUT_FACTOR = 8
+L2_FLUSHED = "flushed between steps (512 MiB write)"
+# GPU spin before a step that is not preceded by the flush (about 100 us at
+# 2 GHz, as long as the flush): the host queues the step meanwhile, so the
+# events do not time the host's launch calls
+SPIN_CYCLES = 200_000
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged-prefill µs/step and attention TFLOP/s (fraction of GB300 bf16 tensor peak)"
@@ -205,13 +219,35 @@ def max_over_ranks(x: float, world: int) -> float:
     return float(t.item())
 
 
+def large_inputs(wl) -> bool:
+    """The decode step's distinct K/V bytes (a shared prefix counted once) are
+    at least LARGE_INPUT_FACTOR times the L2."""
+    return wl.unique_kv_bytes() >= LARGE_INPUT_FACTOR * L2_BYTES
+
+
+def l2_note(wl) -> str:
+    if large_inputs(wl):
+        return (f"not flushed: inputs larger than L2 (the step reads "
+                f"{wl.unique_kv_bytes() / L2_BYTES:.0f}x the 129 MB L2 in distinct K/V bytes)")
+    return L2_FLUSHED
+
+
+def between_steps(flush):
+    """Queue what precedes each timed step: the L2 flush, or (flush None) a
+    GPU spin of about the same length."""
+    if flush is None:
+        torch.cuda._sleep(SPIN_CYCLES)
+    else:
+        flush.zero_()
+
+
 def workload_config(wl, q_len=1, layout="token_major"):
     s = wl.spec
     return {"workload": s.name, "num_seqs": wl.num_seqs, "num_q_heads": s.num_q_heads,
             "num_kv_heads": s.num_kv_heads, "head_dim": s.head_dim, "block_size": s.block_size,
             "num_blocks": wl.num_blocks, "store_rows": int(wl.slot_mapping.shape[0]),
             "context_tokens": int(wl.context_lens.astype(np.int64).sum()),
-            "max_context_len": wl.max_context_len, "seed": wl.seed, "l2": L2_NOTE,
+            "max_context_len": wl.max_context_len, "seed": wl.seed, "l2": l2_note(wl),
             "q_len": q_len, "layout": layout}
 
 
@@ -409,19 +445,19 @@ class DecodeStep:
 
 
 def time_decode(st: DecodeStep, flush, stream, steps, warmup, world):
-    """Store + decode per step with the L2 flushed before each step: one pass
-    through the one-call step (the step time) and one with an event between
-    separate store and decode calls (the split). Returns milliseconds (max
-    over ranks) and the step times."""
+    """Store + decode per step, each step preceded by the L2 flush (or, with
+    flush None, by a GPU spin): one pass through the one-call step (the step
+    time) and one with an event between separate store and decode calls (the
+    split). Returns milliseconds (max over ranks) and the step times."""
     for _ in range(warmup):
-        flush.zero_()
+        between_steps(flush)
         st.step()
     torch.cuda.synchronize()
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(steps)]
     barrier(world)
     torch.cuda.synchronize()
     for i in range(steps):
-        flush.zero_()
+        between_steps(flush)
         ev[i][0].record(stream)
         st.step()
         ev[i][1].record(stream)
@@ -433,7 +469,7 @@ def time_decode(st: DecodeStep, flush, stream, steps, warmup, world):
     ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(steps)]
     torch.cuda.synchronize()
     for i in range(steps):
-        flush.zero_()
+        between_steps(flush)
         ev[i][0].record(stream)
         st.store()
         ev[i][1].record(stream)
@@ -474,13 +510,26 @@ def decode_rates(st: DecodeStep, t):
     }
 
 
+def l2_alt_record(st: DecodeStep, t, flushed: bool):
+    """The step timed in the other L2 mode than its own (see l2_note)."""
+    r = decode_rates(st, t)
+    return {"l2": L2_FLUSHED if flushed else
+            "not flushed (inputs at or below a few times the L2 partly stay there)",
+            "us_per_step": r["us_per_step"], "decode_us": r["decode_us"],
+            "hbm_frac": r["hbm_frac"] if flushed else None}
+
+
 def decode_sub_record(name, args, dev, flush, stream, world):
     workload, q_len, layout = SUB_DECODE[name]
     wl = inputs.generate(workload_spec(args, workload), seed=0, device=dev)
     st = DecodeStep(wl, dev, layout, q_len)
-    t = time_decode(st, flush, stream, args.steps, args.warmup, world)
+    big = large_inputs(wl)
+    t = time_decode(st, None if big else flush, stream, args.steps, args.warmup, world)
     rec = {"config": workload_config(wl, q_len, layout), **decode_rates(st, t),
            "gpu_launches": args.steps * st.launches_per_step()}
+    if big:   # the flushed figure beside it
+        rec["l2_alt"] = l2_alt_record(
+            st, time_decode(st, flush, stream, args.steps, args.warmup, world), True)
     del st, wl
     torch.cuda.empty_cache()
     return rec
@@ -501,23 +550,15 @@ def run_gpu(args, rank, world, local):
     clocks.wait_first_sample()
 
     # ---- device-resident timing: store then decode back to back, as a user
-    # issues them (the decode launch may overlap the store's tail)
-    t = time_decode(st, flush, stream, args.steps, args.warmup, world)
-
-    # ---- warm: the same steps without the L2 flush between them (inputs that
-    # fit L2 then stay there; informative, not the reported value). A short
-    # spin on the GPU before each step stands in for the flush kernel's other
-    # role: the host queues the step while it runs, so the events do not time
-    # the host's launch calls.
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(args.steps)]
-    torch.cuda.synchronize()
-    for i in range(args.steps):
-        torch.cuda._sleep(100_000)
-        ev[i][0].record(stream)
-        st.step()
-        ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    warm_avg = max_over_ranks(sum(e[0].elapsed_time(e[1]) for e in ev) / args.steps, world)
+    # issues them (the decode launch may overlap the store's tail). A step
+    # whose inputs are many times the L2 runs without the flush (l2_note);
+    # every other pass below takes the same mode.
+    fl = None if large_inputs(wl) else flush
+    t = time_decode(st, fl, stream, args.steps, args.warmup, world)
+    # ---- the same in the other mode: flushed for large inputs, else warm
+    # (not flushed; informative, not the reported value)
+    t_alt = time_decode(st, flush if fl is None else None, stream, args.steps, args.warmup,
+                        world)
 
     # ---- end to end through host buffers: the step's inputs are packed in one
     # pinned staging buffer, copied in one transfer, and the output read back
@@ -544,12 +585,12 @@ def run_gpu(args, rank, world, local):
         hout.copy_(st.out, non_blocking=True)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        between_steps(fl)
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = []
     for _ in range(args.steps):
-        flush.zero_()
+        between_steps(fl)
         a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a_.record(stream)
         e2e_step()
@@ -564,12 +605,12 @@ def run_gpu(args, rank, world, local):
     # ---- the same two steps replayed from CUDA graphs (one launch per step)
     def time_replay(g):
         for _ in range(args.warmup):
-            flush.zero_()
+            between_steps(fl)
             g.replay()
         torch.cuda.synchronize()
         ts = []
         for _ in range(args.steps):
-            flush.zero_()
+            between_steps(fl)
             a_, b_ = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             a_.record(stream)
             g.replay()
@@ -601,6 +642,7 @@ def run_gpu(args, rank, world, local):
     wl_struct = dataclasses.replace(wl, q=None, k_new=None, v_new=None, k_cache=None,
                                     v_cache=None)
     rates = decode_rates(st, t)
+    alt_rec = l2_alt_record(st, t_alt, fl is None)
     config = workload_config(wl, st.Q, args.layout)
     launches = args.steps * st.launches_per_step()
     del st, wl, views, dq, dk, dv, ds, dbt, dcl, d_stage
@@ -624,7 +666,7 @@ def run_gpu(args, rank, world, local):
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic", "config": config,
         **{k: v for k, v in rates.items() if k != "us_per_step"},
-        "warm_us_per_step": warm_avg * 1e3,
+        "l2_alt": alt_rec,
         "e2e": {"value": e2e * 1e3, "unit": "us/step", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h},
         "graph": {"us_per_step": graph_ms * 1e3 if args.q_len == 1 else None,
@@ -634,7 +676,8 @@ def run_gpu(args, rank, world, local):
         "gpu_launches": launches,
         "timing": "value: one pa_decode_step call (store, then decode) per step; store_us / "
                   "decode_us: a second pass with separate store and decode calls and an event "
-                  "between them; workloads: the same two passes on each other step",
+                  "between them; config.l2: what precedes each timed step; l2_alt: the same "
+                  "two passes in the other L2 mode; workloads: the same on each other step",
         "clocks": clk,
         "workloads": subs,
     }
@@ -656,6 +699,7 @@ def prefill_flops(pb) -> int:
 def prefill_config(pb, chunk, layout="token_major"):
     c = workload_config(pb.wl, 1, layout)
     c.pop("q_len")
+    c["l2"] = L2_FLUSHED
     c.update(store_rows=int(pb.slot_mapping.shape[0]), query_rows=int(pb.query_start_loc[-1]),
              max_query_len=pb.max_query_len, chunk="whole prompt" if chunk is None else chunk,
              causal_pairs=pb.causal_pairs())
