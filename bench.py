@@ -9,7 +9,9 @@ long-context decode step (8 sequences of 32k-131k tokens among 120 short
 ones, 32 q / 8 KV heads), the largest of the decode steps. Its 2.3 GB of K/V
 reads are 18x the L2, so its steps run back to back (inputs larger than L2);
 steps that read less than 8x the L2 are preceded by an L2 flush (a 512 MiB
-write), and ``l2_alt`` gives each large step flushed as well.
+write). ``l2_alt`` repeats each decode step in the other mode: the large
+steps flushed, the others warm (no flush: inputs near or below the L2 size
+then partly stay in it, so it gives no DRAM fraction).
 ``roofline`` reports the decode launch's KV-read bandwidth against the
 measured HBM copy peak; ``e2e`` repeats the step through host buffers (pinned
 H2D of the step's inputs and D2H of its output inside the timed region);
@@ -49,6 +51,7 @@ DEFAULT_WORKLOAD = "long_context"
 SUB_DECODE = {
     "large_batch": ("large_batch", 1, "token_major"),
     "qwen3_0_6b": ("qwen3_0_6b", 1, "token_major"),
+    "qwen3_0_6b_bs256": ("qwen3_0_6b_bs256", 1, "token_major"),
     "prefix_shared": ("prefix_shared", 1, "token_major"),
     "tiny": ("tiny", 1, "token_major"),
     # multi-token decode: 4 new tokens per sequence (speculative verification)
@@ -527,9 +530,9 @@ def decode_sub_record(name, args, dev, flush, stream, world):
     t = time_decode(st, None if big else flush, stream, args.steps, args.warmup, world)
     rec = {"config": workload_config(wl, q_len, layout), **decode_rates(st, t),
            "gpu_launches": args.steps * st.launches_per_step()}
-    if big:   # the flushed figure beside it
-        rec["l2_alt"] = l2_alt_record(
-            st, time_decode(st, flush, stream, args.steps, args.warmup, world), True)
+    # the other L2 mode beside it: flushed for large inputs, warm for the rest
+    rec["l2_alt"] = l2_alt_record(
+        st, time_decode(st, flush if big else None, stream, args.steps, args.warmup, world), big)
     del st, wl
     torch.cuda.empty_cache()
     return rec
