@@ -142,7 +142,9 @@ PA_API size_t pa_decode_workspace_size(int num_q_heads, int num_kv_heads, int he
  * size num_q_heads / num_kv_heads <= 16; block_size a power of two in
  * [16, 256]; q, k_cache, v_cache, out 16-byte aligned; workspace of at least
  * pa_decode_workspace_size(num_q_heads, num_kv_heads, head_dim, 0) bytes,
- * 16-byte aligned.
+ * 16-byte aligned; num_blocks * block_size and num_blocks * num_kv_heads
+ * below 2^31 (the tile copies address pool rows with 32-bit coordinates;
+ * PA_ERR_UNSUPPORTED otherwise).
  */
 PA_API pa_status_t pa_decode(const void *q, const void *k_cache, const void *v_cache,
                       const int32_t *block_tables, int max_blocks_per_seq,
@@ -312,7 +314,9 @@ PA_API pa_status_t pa_decode_step(const void *k, const void *v, const int64_t *s
  * block table. A row with no visible token outputs zero. max_query_len is a
  * host-side hint for the grid (the largest n_s; a smaller value is still
  * correct, only slower). Token-major pool layout; group size <= 16; head_dim
- * 128. Computes in fp32 on the tensor cores, output bf16. Allocates nothing.
+ * 128; num_seqs and num_kv_heads at most 65535; the pool-size limit of
+ * pa_decode. Computes in fp32 on the tensor cores, output bf16. Allocates
+ * nothing.
  */
 PA_API pa_status_t pa_prefill(const void *q, const void *k_cache, const void *v_cache,
                               const int32_t *block_tables, int max_blocks_per_seq,

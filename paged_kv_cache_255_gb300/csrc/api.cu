@@ -37,6 +37,14 @@ class TraceRange {
 
 bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// The TMA tile copies address the pool's rows with int32 coordinates: token
+// rows (num_blocks * block_size) in the token-major map, (block, KV head)
+// rows (num_blocks * num_kv_heads) in the head-major one.
+bool pool_rows_fit(int64_t num_blocks, int block_size, int num_kv_heads) {
+    return num_blocks * block_size < ((int64_t)1 << 31) &&
+           num_blocks * num_kv_heads < ((int64_t)1 << 31);
+}
+
 int log2_exact(int x) {
     int l = 0;
     while ((1 << l) < x) ++l;
@@ -188,6 +196,7 @@ pa_status_t prefill_impl(const void *q, const void *k_cache, const void *v_cache
         return PA_ERR_INVALID_ARG;
     if (max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_INVALID_ARG;
     if (num_seqs > 65535 || num_kv_heads > 65535) return PA_ERR_UNSUPPORTED;
+    if (!pool_rows_fit(num_blocks, block_size, num_kv_heads)) return PA_ERR_UNSUPPORTED;
     pa::PrefillArgs a{};
     a.q = q;
     a.k_cache = k_cache;
@@ -262,10 +271,7 @@ pa_status_t decode_check_args(const void *q, const void *k_cache, const void *v_
     if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
         return PA_ERR_INVALID_ARG;
     if (max_blocks_per_seq == 0 || num_blocks == 0) return PA_ERR_INVALID_ARG;
-    // the tile copies address pool rows with int32 coordinates
-    if (num_blocks * block_size >= ((int64_t)1 << 31) ||
-        num_blocks * num_kv_heads >= ((int64_t)1 << 31))
-        return PA_ERR_UNSUPPORTED;
+    if (!pool_rows_fit(num_blocks, block_size, num_kv_heads)) return PA_ERR_UNSUPPORTED;
     return PA_OK;
 }
 

@@ -63,6 +63,8 @@ def _decode(pa_lib, **over):
     (dict(scale=float("nan")), pa.PA_ERR_INVALID_ARG),
     (dict(mb=0), pa.PA_ERR_INVALID_ARG),
     (dict(S=0, q=NULL, out=NULL), pa.PA_OK),        # empty batch: nothing to do
+    (dict(NB=1 << 27), pa.PA_ERR_UNSUPPORTED),      # 2^31 token rows: past 32-bit coordinates
+    (dict(NB=1 << 26, Hq=32, Hkv=32), pa.PA_ERR_UNSUPPORTED),  # 2^31 (block, head) rows
 ])
 def test_decode_host_checks(pa_lib, over, want):
     assert _decode(pa_lib, **over) == want
@@ -144,6 +146,8 @@ def test_workspace_size_rejects_bad_heads(pa_lib):
     (dict(Hq=70000 * 2, Hkv=70000), pa.PA_ERR_UNSUPPORTED),
     (dict(S=0, q=NULL, out=NULL, qsl=NULL), pa.PA_OK),   # empty batch
     (dict(T=0, q=NULL, out=NULL), pa.PA_OK),             # no query rows
+    (dict(NB=1 << 27), pa.PA_ERR_UNSUPPORTED),           # pool rows past 32-bit coordinates
+    (dict(NB=1 << 26, Hq=32, Hkv=32), pa.PA_ERR_UNSUPPORTED),
 ])
 def test_prefill_host_checks(pa_lib, over, want):
     a = dict(q=16, k=16, v=16, bt=16, mb=4, cl=16, qsl=16, mql=8, scale=0.1, out=16, S=2, T=20,
