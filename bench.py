@@ -78,17 +78,20 @@ FALLBACK_BF16_TFLOPS = 1900.0
 PREFILL_METRIC = "paged-prefill µs/step and attention TFLOP/s (fraction of GB300 bf16 tensor peak)"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 KERNEL_SOURCES = ["paged_kv_cache_255_gb300/csrc/decode.cu", "paged_kv_cache_255_gb300/csrc/common.cuh"]
+PREFILL_SOURCES = ["paged_kv_cache_255_gb300/csrc/prefill_tc.cu",
+                   "paged_kv_cache_255_gb300/csrc/tcgen05.cuh",
+                   "paged_kv_cache_255_gb300/csrc/common.cuh"]
 # a whole oracle step is timed unless one all-cores step would take longer
 # than this; then a sample of the step's outputs is timed and scaled
 FULL_STEP_LIMIT_S = 30.0
 
 
-def kernel_hash() -> str:
-    """Hash of the decode kernel's code (comments and whitespace removed, so
-    that an edited comment does not invalidate counters taken on the same
-    code)."""
+def kernel_hash(sources=KERNEL_SOURCES) -> str:
+    """Hash of a kernel's code, by default the decode kernel's (comments and
+    whitespace removed, so that an edited comment does not invalidate
+    counters taken on the same code)."""
     h = hashlib.sha256()
-    for p in KERNEL_SOURCES:
+    for p in sources:
         with open(os.path.join(ROOT, p)) as f:
             text = f.read()
         text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
@@ -107,14 +110,15 @@ def measured_peaks(key="hbm_gbs"):
         return {"hbm_gbs": FALLBACK_HBM_GBS, "bf16_tflops": FALLBACK_BF16_TFLOPS}[key], "fallback"
 
 
-def ncu_traffic(workload: str):
-    """DRAM bytes per decode launch from the committed ncu summary, if it was
-    taken on this workload with the current kernel source."""
+def ncu_traffic(workload: str, sources=KERNEL_SOURCES):
+    """DRAM bytes per launch of the kernel built from `sources` (the decode
+    kernel by default) from the committed ncu summary, if it was taken on this
+    workload key with the current kernel source."""
     try:
         text = open(PROFILE_FILE).read()
     except OSError:
         return None
-    want = kernel_hash()
+    want = kernel_hash(sources)
     for m in re.finditer(r"^traffic\s+workload=(\S+)\s+kernel_hash=(\S+)\s+bytes_per_launch=(\d+)",
                          text, re.M):
         if m.group(1) == workload and m.group(2) == want:
@@ -486,6 +490,12 @@ def time_decode(st: DecodeStep, flush, stream, steps, warmup, world):
             "store_ms": max_over_ranks(sum(store_ms) / len(store_ms), world)}
 
 
+def traffic_key(st: DecodeStep) -> str:
+    """Workload key of a decode step's line in the traffic summary."""
+    return (st.wl.spec.name + ("_head_major" if st.HM else "")
+            + (f"_q{st.Q}" if st.Q > 1 else ""))
+
+
 def decode_rates(st: DecodeStep, t):
     """Bandwidth figures of a timed decode step."""
     wl = st.wl
@@ -507,7 +517,7 @@ def decode_rates(st: DecodeStep, t):
         "unique_kv_read_gbs": wl.unique_kv_bytes() / dec_s / 1e9,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak,
-                     "traffic": ncu_traffic(s.name) if st.Q == 1 and not st.HM else None,
+                     "traffic": ncu_traffic(traffic_key(st)),
                      "kernel": "pa_decode (decode + combine launches)",
                      "algorithmic_bytes": kv_bytes, "peak_source": f"{peak_src} hbm_gbs"},
     }
@@ -840,7 +850,9 @@ def prefill_rates(pb, t):
     return {"us_per_step": t["ms"] * 1e3, "store_us": t["store_ms"] * 1e3,
             "prefill_us": t["prefill_ms"] * 1e3,
             "roofline": {"bound": "tensor", "achieved": achieved, "peak": peak, "unit": "TFLOP/s",
-                         "frac": achieved / peak, "traffic": None, "kernel": "pa_prefill",
+                         "frac": achieved / peak,
+                         "traffic": ncu_traffic("prefill_" + pb.wl.spec.name, PREFILL_SOURCES),
+                         "kernel": "pa_prefill",
                          "algorithmic_flops": flops,
                          "peak_source": f"{peak_src} bf16_tflops (burst)"}}
 
