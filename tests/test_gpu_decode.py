@@ -206,3 +206,24 @@ def test_full_size_multi_token_decode():
     rk, rv = O.store_kvcache(wl.k_new.cpu(), wl.v_new.cpu(), host_k, host_v, wl.slot_mapping)
     ref = O.decode_multi(q, rk, rv, wl.block_tables, wl.context_lens, wl.scale)
     gu.assert_close(out, ref, "qwen3 Q=4")
+
+
+def test_million_token_sequence():
+    """A maximum-length step: one sequence of 2^20 tokens among three short
+    ones (32 q / 8 KV heads, bs 16; a block-table row of 65,536 entries), in
+    the benchmark's launch configuration. Each long (sequence, KV head) is cut
+    into about 230 split-K pieces that the combine merges in many batches;
+    the store is checked bit for bit and every output row against the oracle."""
+    spec = inputs.Spec("million", ((1, 1 << 20, 1 << 20), (3, 1, 2000)), 32, 8, 16)
+    wl = inputs.generate(spec, seed=3, device="cuda")
+    host_k, host_v = wl.k_cache.cpu(), wl.v_cache.cpu()
+    out, gkc, gvc = gu.gpu_step(wl)
+    O = oracle.get()
+    kc, vc = O.store_kvcache(wl.k_new.cpu(), wl.v_new.cpu(), host_k, host_v, wl.slot_mapping)
+    assert np.array_equal(gu.host_bits(gkc), kc) and np.array_equal(gu.host_bits(gvc), vc)
+    del gkc, gvc, host_k, host_v
+    S, Hq = wl.q.shape[0], wl.q.shape[1]
+    pairs = np.array([(s, h) for s in range(S) for h in range(Hq)], dtype=np.int32)
+    ref = O.decode_pairs(wl.q.cpu(), kc, vc, wl.block_tables, wl.context_lens, wl.scale, pairs)
+    got = out[torch.from_numpy(pairs[:, 0]).long(), torch.from_numpy(pairs[:, 1]).long()]
+    gu.assert_close(got, ref, "2^20-token sequence")
