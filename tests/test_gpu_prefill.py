@@ -201,6 +201,25 @@ def test_full_size_sampled_rows(name):
     assert torch.isfinite(out.float()).all()
 
 
+def test_long_chunk_over_long_context():
+    """A maximum-size prefill: one sequence of 131,072 tokens takes a chunk of
+    its last 16,384 (32 q / 8 KV heads, so 256 pairs of query tiles per KV
+    head, each reading up to 1024 key tiles), beside a 300-token whole prompt;
+    the persistent CTAs walk thousands of items. The oracle checks sampled rows
+    one by one: the first and last rows of both chunks and 20 random ones."""
+    pb = inputs.prefill_batch(_spec("long_chunk", 32, 8, 16), seed=17,
+                              context_lens=[131072, 300], chunk_lens=[16384, 300])
+    d = _device(pb)
+    out = _gpu_step(pb, d, max_query_len=pb.max_query_len)
+    qsl = pb.query_start_loc
+    rng = np.random.Generator(np.random.PCG64(71))
+    rows = np.unique(np.concatenate([qsl[:-1], qsl[1:] - 1,
+                                     rng.integers(0, qsl[-1], size=20)])).astype(np.int64)
+    ref = _sampled_rows_ref(pb, d["k_cache"].cpu(), d["v_cache"].cpu(), rows)
+    gu.assert_close(out[torch.from_numpy(rows).cuda()], ref, "16k-row chunk over 128k tokens")
+    assert torch.isfinite(out.float()).all()
+
+
 def test_launches_on_two_streams_at_once():
     """Persistent CTAs take over only CTAs of their own grid: two prefill
     launches running at the same time on two streams, each grid several times
