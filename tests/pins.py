@@ -386,7 +386,23 @@ def pin_prefill_is_multi_token(O):
     assert np.array_equal(a, b.reshape(a.shape))
 
 
+def pin_pairs_sdpa(O):
+    """decode_pairs (the sampled outputs the full-size GPU checks use) on a
+    shuffled list of (sequence, head) pairs with repeats: each output is that
+    row of fp64 SDPA over the sequence's contiguous K/V."""
+    spec = inputs.scaled(inputs.SPECS["large_batch"], num_seqs=6, ctx_div=16, name="pairs_small")
+    wl = inputs.generate(spec, seed=4, keep_content=True)
+    _, kc, vc = run_step(O, wl)
+    ref = sdpa_reference(wl)
+    rng = np.random.Generator(np.random.PCG64(8))
+    S, Hq = wl.num_seqs, spec.num_q_heads
+    pairs = np.stack([rng.integers(0, S, 40), rng.integers(0, Hq, 40)], axis=1).astype(np.int32)
+    got = O.decode_pairs(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale, pairs)
+    err = np.abs(got - ref[pairs[:, 0], pairs[:, 1]]).max()
+    assert err <= 1e-10, f"decode_pairs vs fp64 SDPA max err {err}"
+
+
 ALL_PINS = [pin_sdpa, pin_single_token, pin_zero_keys, pin_unit_values, pin_three_tokens,
             pin_dominant_key, pin_renumbering, pin_prefix_private, pin_block_size,
             pin_nan_free, pin_store, pin_multi_sdpa, pin_multi_prefix, pin_head_major,
-            pin_prefill_sdpa, pin_prefill_is_multi_token]
+            pin_prefill_sdpa, pin_prefill_is_multi_token, pin_pairs_sdpa]

@@ -45,6 +45,13 @@ MUTANTS = [
      "const int i = row;"),
     ("prefill_boundary_row_to_previous_sequence", "while (query_start_loc[s + 1] <= row)",
      "while (query_start_loc[s + 1] < row)"),
+    # decode_pairs, the oracle of the full-size GPU checks
+    ("pairs_length_of_first_sequence", "context_lens[pairs[2 * i]], ORACLE_LAYOUT_TOKEN_MAJOR,",
+     "context_lens[0], ORACLE_LAYOUT_TOKEN_MAJOR,"),
+    ("pairs_query_of_first_sequence", "num_blocks, pairs[2 * i],\n",
+     "num_blocks, 0,\n"),
+    ("pairs_outputs_reversed", "context_lens[pairs[2 * i]], ORACLE_LAYOUT_TOKEN_MAJOR,\n                           out + i * head_dim);",
+     "context_lens[pairs[2 * i]], ORACLE_LAYOUT_TOKEN_MAJOR,\n                           out + (num_pairs - 1 - i) * head_dim);"),
 ]
 
 
