@@ -75,6 +75,8 @@ L2_FLUSHED = "flushed between steps (512 MiB write)"
 SPIN_CYCLES = 200_000
 FALLBACK_HBM_GBS = 6800.0
 FALLBACK_BF16_TFLOPS = 1900.0
+# comparison kernels selectable with --variant: name -> pagedattn flag
+VARIANTS = {"decode_simt": "VARIANT_DECODE_SIMT", "prefill_mma": "VARIANT_PREFILL_MMA"}
 PREFILL_METRIC = "paged-prefill µs/step and attention TFLOP/s (fraction of GB300 bf16 tensor peak)"
 PROFILE_FILE = os.path.join(ROOT, "profiles", "decode_traffic.txt")
 KERNEL_SOURCES = ["paged_kv_cache_255_gb300/csrc/decode.cu", "paged_kv_cache_255_gb300/csrc/common.cuh"]
@@ -694,6 +696,8 @@ def run_gpu(args, rank, world, local):
         "clocks": clk,
         "workloads": subs,
     }
+    if args.variant:
+        line["kernel_variant"] = args.variant
     if host is not None:
         line["cpu_baseline"] = cpu_baseline(wl_struct, host)
     print(json.dumps(line), flush=True)
@@ -940,6 +944,8 @@ def run_gpu_prefill(args, rank, world, local):
         "timing": "value: store + prefill per step, events between the two calls",
         "clocks": clk,
     }
+    if args.variant:
+        line["kernel_variant"] = args.variant
     if not args.no_cpu_baseline:
         us, threads, sample = prefill_oracle_sample(pb, args.cpu_seconds)
         line["cpu_baseline"] = {"value": us, "unit": "us/step", "cores": threads,
@@ -968,10 +974,18 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-sub-records", action="store_true",
                     help="time the chosen workload only (profiling runs)")
+    ap.add_argument("--variant", choices=sorted(VARIANTS),
+                    help="run a comparison kernel the library keeps for tests instead of the "
+                         "product kernel (profiling runs; the line then names it)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
+    if args.variant and (args.impl != "native" or not torch.cuda.is_available()):
+        ap.error("--variant selects a GPU kernel")
     rank, world, local = dist_setup(args.gpus)
+    if args.variant:
+        from paged_kv_cache_255_gb300 import pagedattn as pa
+        pa.debug_kernel_variant(getattr(pa, VARIANTS[args.variant]))
     prefill = args.workload in inputs.PREFILL_SPECS
     if args.impl == "reference":
         (run_reference_prefill if prefill else run_reference)(args, rank, world)
