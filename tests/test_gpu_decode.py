@@ -208,6 +208,26 @@ def test_full_size_multi_token_decode():
     gu.assert_close(out, ref, "qwen3 Q=4")
 
 
+@pytest.mark.parametrize("scale", [0.0, -0.08838834764831845, 1.0])
+def test_decode_scales(scale, kernel):
+    """Scale edge cases on both tile computations: zero (every weight equal,
+    the output the mean of the V rows), negative (the softmax of the negated
+    scores: the running minimum of the raw scores leads), and 1.0, eleven
+    times the usual 1/sqrt(128) (sharp weights and large running-max jumps
+    between tiles); store then decode against the oracle."""
+    wl = inputs.generate(SMALL["large_small"], seed=5)
+    O = oracle.get()
+    kc, vc = O.store_kvcache(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping)
+    ref = O.decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, scale)
+    d = gu.device_inputs(wl)
+    pa.store_kvcache(d["k_new"], d["v_new"], d["k_cache"], d["v_cache"], d["slot_mapping"])
+    out = pa.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], d["context_lens"],
+                    scale)
+    torch.cuda.synchronize()
+    assert pa.take_device_error() == 0
+    gu.assert_close(out, ref, f"scale {scale}")
+
+
 def test_million_token_sequence():
     """A maximum-length step: one sequence of 2^20 tokens among three short
     ones (32 q / 8 KV heads, bs 16; a block-table row of 65,536 entries), in
