@@ -109,3 +109,18 @@ def test_many_short_sequences():
     out, gkc, gvc = gu.gpu_step(wl)
     assert np.array_equal(gu.host_bits(gkc), kc) and np.array_equal(gu.host_bits(gvc), vc)
     gu.assert_close(out, ref, "3000 short sequences")
+
+
+def test_sequence_count_past_16_bits():
+    """70,000 sequences of 0..40 tokens (2 q heads / 1 KV head, bs 16): more
+    sequences than a 16-bit index holds; the share planning scans the lengths
+    in about 550 chunks per CTA, and every output and the pool after the
+    store are checked."""
+    spec = inputs.Spec("many_seqs", ((70000, 0, 40),), 2, 1, 16)
+    wl = inputs.generate(spec, seed=9)
+    O = oracle.get()
+    kc, vc = O.store_kvcache(wl.k_new, wl.v_new, wl.k_cache, wl.v_cache, wl.slot_mapping)
+    ref = O.decode(wl.q, kc, vc, wl.block_tables, wl.context_lens, wl.scale)
+    out, gkc, gvc = gu.gpu_step(wl)
+    assert np.array_equal(gu.host_bits(gkc), kc) and np.array_equal(gu.host_bits(gvc), vc)
+    gu.assert_close(out, ref, "70,000 sequences")
