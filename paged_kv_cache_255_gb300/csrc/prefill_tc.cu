@@ -749,7 +749,9 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
         const uint32_t hi = (uint32_t)(dq >> 32);                           // same for all three
         const uint32_t q_lo = (uint32_t)dq, k_lo = (uint32_t)dk, v_lo = (uint32_t)dv;
         auto desc = [hi](uint32_t lo) { return ((uint64_t)hi << 32) | lo; };
-        // S_t = Q_t K^T from K stage st
+        // S_t = Q_t K^T from K stage st. The elected lane issues; the other
+        // lanes go on to the next barrier test, whose warp-wide vote waits
+        // for it (a __syncwarp after each batch measured 0.4-1.3 % slower).
         auto issue_s = [&](int t, int st, uint32_t release) {
             const uint32_t qd = q_lo + t * (kQBytes >> 4);
             const uint32_t kd = k_lo + st * (kKVBytes >> 4);
@@ -763,7 +765,6 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 tc::commit(bar(kBarSFull + t));
                 if (release) tc::commit(release);
             }
-            __syncwarp();
         };
         // O_t += P_t V over the first nv 16-key groups of V stage st (P_t in
         // TMEM, 8 columns per 16 keys; the groups past the end of the keys
@@ -781,7 +782,6 @@ prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap tmap_
                 tc::commit(bar(kBarPVDone + t));
                 if (release) tc::commit(release);
             }
-            __syncwarp();
         };
         // every lane tests the barrier (one shared-memory access for the
         // warp, no divergent branch) and a vote gives the warp one answer: a
