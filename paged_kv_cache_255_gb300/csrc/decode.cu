@@ -18,9 +18,9 @@
 //     CTA plans the split from context_lens in its prologue (before waiting on
 //     the previous kernel when that is the same step's store).
 //   * A worker streams its tiles through a private kStages-deep ring in shared
-//     memory. One lane fills a stage with four TMA boxes (the K tile and the
-//     V tile, each 16 rows x 64 head dims twice, 128-byte swizzle) counted
-//     on the stage's mbarrier; every lane then waits on that barrier. A
+//     memory. One lane fills a stage with two TMA boxes (the K tile and the
+//     V tile, each 16 rows x 128 head dims landing as two 64-dim halves,
+//     128-byte swizzle) counted on the stage's mbarrier; every lane then waits on that barrier. A
 //     tile with no tokens, or with a block id outside the pool, is
 //     zero-filled by the warp instead, and the V rows of a sequence's last,
 //     partly used tile are zeroed after they land. Per query head of its KV
@@ -53,7 +53,7 @@ constexpr int kWarps = 4;      // workers per CTA
 // ring this shallow, three CTAs fit an SM (12 warps), which measured faster
 // than two CTAs of three-stage rings.
 constexpr int kStages = 2;
-constexpr int kBoxBytes = kTileBytes / 2;     // one TMA box: 16 rows x 128 B (64 head dims)
+constexpr int kBoxBytes = kTileBytes / 2;     // one half of a tile: 16 rows x 128 B (64 head dims)
 constexpr int kStageBytes = 2 * kTileBytes;   // K tile then V tile
 constexpr int kRingBytes = kStages * kStageBytes;
 constexpr int kCombineBatch = 8;              // pieces a combine warp loads at once
@@ -61,7 +61,7 @@ constexpr float kNegInf = -INFINITY;
 constexpr unsigned long long kWaitLimitNs = 1000000000ull;   // bounded waits give up after 1 s
 
 // Byte offset, inside a K or V tile in shared memory, of the 16-byte chunk
-// holding head dims [8c, 8c + 8) of token row r. The tile is two TMA boxes
+// holding head dims [8c, 8c + 8) of token row r. The tile lands as two halves
 // (dims 0-63, then 64-127) of 16 rows x 128 B in the 128-byte swizzle: chunk
 // k of a 128-byte row r sits at position k ^ (r % 8).
 __device__ __forceinline__ uint32_t chunk_off(int r, int c) {
@@ -143,7 +143,7 @@ __device__ __forceinline__ int tile_block(const Cursor &c, const DecodeArgs &a) 
 }
 
 // Fill `stage` with the K tile and the V tile under cursor c (physical block
-// bid): two TMA boxes each, issued by one elected lane and counted in bytes on `bar`.
+// bid): one TMA box each, issued by one elected lane and counted in bytes on `bar`.
 // A tile with no tokens, or whose block id lies outside the pool, is written
 // with zeros by the warp instead (each of its keys then scores 0 and adds a
 // zero value) and `bar` gets a plain arrival. The stage's previous contents
@@ -160,18 +160,15 @@ __device__ __forceinline__ void issue_tile(const Cursor &c, int bid, uint8_t *st
         // from an elected lane rather than under lane == 0 the step measured
         // 1-5 % faster
         if (tc::elect_one()) {
-            // token-major pool: (x, KV head, block * bs + offset); head-major
-            // pool: (x, offset, block * Hkv + KV head)
+            // token-major pool: (0, block * bs + offset, 0, KV head);
+            // head-major pool: (0, offset, 0, block * Hkv + KV head)
             const int off = (c.j << 4) & ((1 << a.block_size_log2) - 1);
-            const int c1 = a.head_major ? off : c.kvh;
-            const int c2 = a.head_major ? bid * a.num_kv_heads + c.kvh
-                                        : (bid << a.block_size_log2) + off;
+            const int row = a.head_major ? off : (bid << a.block_size_log2) + off;
+            const int outer = a.head_major ? bid * a.num_kv_heads + c.kvh : c.kvh;
             const uint32_t dst = smem_u32(stage);
             mbar_arrive_expect_tx(bar, kStageBytes);
-            tc::tma_load_3d(dst, mk, 0, c1, c2, bar);
-            tc::tma_load_3d(dst + kBoxBytes, mk, 64, c1, c2, bar);
-            tc::tma_load_3d(dst + kTileBytes, mv, 0, c1, c2, bar);
-            tc::tma_load_3d(dst + kTileBytes + kBoxBytes, mv, 64, c1, c2, bar);
+            tc::tma_load_4d(dst, mk, 0, row, 0, outer, bar);               // K tile
+            tc::tma_load_4d(dst + kTileBytes, mv, 0, row, 0, outer, bar);  // V tile
         }
     } else {
         uint4 *z = reinterpret_cast<uint4 *>(stage);
@@ -893,8 +890,8 @@ struct Launcher {
         if (e != cudaSuccess) return e;
         CUtensorMap mk, mv;
         const int bs = 1 << a.block_size_log2;
-        if (!make_pool_map(&mk, a.k_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0) ||
-            !make_pool_map(&mv, a.v_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0))
+        if (!make_tile_map(&mk, a.k_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0) ||
+            !make_tile_map(&mv, a.v_cache, a.num_blocks, bs, a.num_kv_heads, a.head_major != 0))
             return cudaErrorInvalidValue;
         const unsigned grid = (a.num_workers + kWarps - 1) / kWarps;
         DecodeArgs args_copy = a;

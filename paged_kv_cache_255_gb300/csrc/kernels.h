@@ -129,6 +129,13 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder();
 bool make_pool_map(CUtensorMap *m, const void *pool, int64_t num_blocks, int block_size,
                    int num_kv_heads, bool head_major);
 
+// TMA tensor map over a K or V pool whose one box is a whole 16-token tile of
+// one KV head (both 64-dim halves, the same landing layout as two boxes of
+// make_pool_map's map). Coordinates: token-major (0, block * bs + offset, 0,
+// KV head); head-major (0, offset, 0, block * Hkv + KV head).
+bool make_tile_map(CUtensorMap *m, const void *pool, int64_t num_blocks, int block_size,
+                   int num_kv_heads, bool head_major);
+
 cudaError_t launch_store_kvcache(const void *k, const void *v, void *k_cache, void *v_cache,
                                  const int64_t *slot_mapping, int64_t num_tokens,
                                  int num_kv_heads, int head_dim, int block_size_log2,
