@@ -98,6 +98,29 @@ def test_decode_never_reads_entries_past_the_last_block():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
+@pytest.mark.parametrize("kernel", ["mma", "simt"])
+def test_decode_clamps_lengths_to_the_table(kernel):
+    """A length below zero or past what its block-table row can hold is
+    clamped to [0, max_blocks_per_seq * block_size], as the header states: a
+    negative length gives a zero output, and a sequence whose row is full,
+    given 1000 tokens more than the row holds, reads exactly its row. Nothing
+    is recorded (clamping is defined behaviour, not an error)."""
+    gu.decode_kernel(kernel)
+    spec = inputs.Spec("clamp", ((4, 1, 1),), 16, 8, 16, store_mode="none")
+    wl = inputs.generate(spec, seed=21, context_lens=[320, 100, 37, 250])
+    cap = wl.block_tables.shape[1] * spec.block_size
+    assert cap == 320                                    # sequence 0 fills its row
+    ref = oracle.get().decode(wl.q, wl.k_cache, wl.v_cache, wl.block_tables,
+                              np.array([320, 0, 37, 250], np.int32), wl.scale)
+    d = gu.device_inputs(wl)
+    cl = torch.tensor([cap + 1000, -5, 37, 250], dtype=torch.int32, device="cuda")
+    out = pa.decode(d["q"], d["k_cache"], d["v_cache"], d["block_tables"], cl, wl.scale)
+    torch.cuda.synchronize()
+    assert pa.take_device_error() == 0
+    gu.assert_close(out, ref, f"clamped lengths ({kernel})")
+    assert torch.count_nonzero(out[1]).item() == 0
+
+
 @pytest.mark.parametrize("kernel", ["tc", "mma"])
 def test_prefill_reads_out_of_range_block_as_zeros_and_reports(kernel, monkeypatch):
     gu.prefill_kernel(kernel)
